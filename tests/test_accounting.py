@@ -1,0 +1,30 @@
+"""Work counts used by the benchmark, pinned to the counts the lesson prints."""
+import json
+import os
+
+from exact_io_aware_08_gb300 import accounting as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def test_causal_tile_count_matches_page():
+    g = json.load(open(os.path.join(GOLDEN, "causal_and_traffic_counts.json")))["causal_tiles"]
+    assert W.causal_tiles(g["N"], g["B"]) == g["computed"]
+    assert (g["N"] // g["B"]) ** 2 == g["total"]
+
+
+def test_at_scale_counts_match_page():
+    g = json.load(open(os.path.join(GOLDEN, "causal_and_traffic_counts.json")))["at_scale"]
+    n, d = g["N"], g["d"]
+    sig = lambda x: float(f"{x:.{g['printed_sig_figs']}g}")
+    assert sig(W.fwd_flops(1, 1, n, n, d, False)) == g["fwd_flop_per_head"]
+    assert sig(W.standard_traffic_elements(n, d)) == g["standard_traffic_elements_per_head"]
+    assert sig(W.tiled_traffic_elements(n, d, g["Br"])) == g["flash_traffic_elements_per_head_no_cache"]
+    assert g["heads"] * n * 4 == g["lse_bytes_all_heads"]
+
+
+def test_pairs_and_flop_ratios():
+    assert W.pairs(4, 4, True) == 10
+    assert W.pairs(3, 5, False) == 15
+    # the backward is 25% more matmul work than the four plain matmuls (10 vs 8 N^2 d)
+    assert W.bwd_flops(1, 1, 64, 64, 32, False) * 8 == W.fwd_flops(1, 1, 64, 64, 32, False) * 20

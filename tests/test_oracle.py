@@ -1,0 +1,358 @@
+"""Pins for the fp64 oracle: values the pages print, closed forms, invariants, independent
+library routines and finite differences.  None of these retypes the oracle's formulas.
+
+Pages: "FlashAttention and online softmax" (ML Systems lesson 4) -- "Lesson4" below.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as A
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def rng_inputs(seed, B, H, n_q, n_kv, d, dv=None):
+    g = np.random.default_rng(seed)
+    dv = d if dv is None else dv
+    q = g.standard_normal((B, H, n_q, d))
+    k = g.standard_normal((B, H, n_kv, d))
+    v = g.standard_normal((B, H, n_kv, dv))
+    do = g.standard_normal((B, H, n_q, dv))
+    return q, k, v, do
+
+
+# ---------------------------------------------------------------------------------------------
+# Worked examples printed on the pages
+# ---------------------------------------------------------------------------------------------
+
+def test_online_scalar_example_lesson4_small_numbers():
+    g = load("online_scalar_1_2_then_4.json")
+    b1, b2 = g["blocks"]
+    x = np.array(b1 + b2)
+    v = np.zeros_like(x)                      # values do not enter l
+    m, l, o, tr = A.online_softmax(x, v, [(0, 2), (2, 3)])
+    p = g["printed"]
+    nd = g["printed_decimals"]
+    assert round(tr[0][1], nd) == p["l_after_block1"]
+    assert round(tr[1][0], nd) == p["factor_block2"]
+    assert round(tr[1][0] * tr[0][1], nd) == p["rescaled_old_sum"]
+    assert m == p["m_final"]
+    assert round(l, nd) == p["l_final"]
+    # closed form 1 + e^-2 + e^-3
+    assert abs(l - (1 + math.exp(-2) + math.exp(-3))) < 1e-15
+
+
+def test_worked_example_a_online_by_hand():
+    g = load("worked_example_a.json")
+    x = np.log(np.array(g["x_exp"]))
+    v = np.array(g["v"])
+    m, l, o, tr = A.online_softmax(x, v, [tuple(b) for b in g["blocks"]])
+    for (f, lj, oj), want in zip(tr, g["per_block"]):
+        assert abs(f - want["factor"]) < 1e-15
+        assert abs(lj - want["l"]) < 1e-14
+        assert abs(oj - want["o_tilde"]) < 1e-14
+    assert abs(o / l - 44 / 15) < 1e-14
+    assert abs(m + math.log(l) - math.log(15)) < 1e-14
+    # the oracle's plain definition agrees with the page's hand computation too
+    o_def, lse_def, _ = A.forward_head(x[None, :1] * 0 + 1.0, x[:, None], v[:, None], 1.0, False)
+    assert abs(o_def[0, 0] - 44 / 15) < 1e-14
+    assert abs(lse_def[0] - math.log(15)) < 1e-14
+
+
+def test_worked_example_b_merge():
+    g = load("worked_example_b_merge.json")
+    o, lse = A.merge(np.array([4 / 3]), math.log(3), np.array([10 / 3]), math.log(12))
+    assert abs(lse - math.log(15)) < 1e-14
+    assert abs(o[0] - 44 / 15) < 1e-14
+    assert abs(math.exp(math.log(3) - lse) - g["merged"]["w_A"]) < 1e-15
+    assert abs(math.exp(math.log(12) - lse) - g["merged"]["w_B"]) < 1e-15
+    assert abs(o[0] - 7 / 3) > 0.5            # the plain average is wrong
+
+
+def test_check_yourself_q1_q2():
+    g = load("check_yourself.json")
+    q1 = g["q1"]
+    s = q1["state"]
+    m, l, o, f = A.online_step(s["m"], s["l"], s["o_tilde"], q1["block_scores"], q1["block_values"])
+    e2 = math.exp(-2)
+    assert m == 5.0
+    assert abs(l - (1 + 3 * e2)) < 1e-15 and round(l, 3) == q1["answer"]["l_printed"]
+    assert abs(o - (1 + 5 * e2)) < 1e-15 and round(float(o), 3) == q1["answer"]["o_tilde_printed"]
+    assert round(float(o) / l, 3) == q1["answer"]["output_printed"]
+    q2 = g["q2"]
+    o, lse = A.merge(np.array([1.0]), math.log(2), np.array([4.0]), math.log(6))
+    assert abs(lse - math.log(8)) < 1e-15
+    assert abs(o[0] - 3.25) < 1e-15
+
+
+def test_quick_checks_factor_and_merge():
+    g = load("quick_checks.json")
+    # the state after a block with max 3, then a block whose largest score is 5
+    m, l, o, f = A.online_step(-np.inf, 0.0, 0.0, [3.0], [0.0])
+    m, l, o, f = A.online_step(m, l, o, [5.0, 1.0], [0.0, 0.0])
+    assert abs(f - math.exp(3 - 5)) < 1e-16
+    o, lse = A.merge(np.array([2.0]), math.log(1), np.array([5.0]), math.log(3))
+    assert abs(o[0] - 17 / 4) < 1e-15 and abs(lse - math.log(4)) < 1e-15
+
+
+# ---------------------------------------------------------------------------------------------
+# The theorem: online recurrence == three-pass softmax, any block split
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", range(6))
+def test_online_equals_three_pass_random_splits(seed):
+    g = np.random.default_rng(seed)
+    n = int(g.integers(1, 300))
+    x = g.standard_normal(n) * (1 + 10 * seed)
+    v = g.standard_normal((n, 5))
+    cuts = sorted(set(g.integers(0, n + 1, size=int(g.integers(0, 12))).tolist()) | {0, n})
+    bounds = list(zip(cuts[:-1], cuts[1:]))
+    m, l, o, _ = A.online_softmax(x, v, bounds)
+    p, m3, l3 = A.three_pass_softmax(x[None, :])
+    assert m == m3[0]
+    np.testing.assert_allclose(o / l, (p @ v)[0], rtol=0, atol=1e-13)
+    assert abs((m + math.log(l)) - A.lse_from(m3, l3)[0]) < 1e-12
+
+
+def test_page_numpy_tiled_check_n100_d32():
+    """Lesson4 §5 'In code': a tiled pass over N=100 (not a multiple of the 16 tile), d=32
+    must match the plain definition to 1e-12, causal and not."""
+    g = np.random.default_rng(0)
+    Q, K, V = (g.normal(size=(100, 32)) for _ in range(3))
+    tau = 1 / math.sqrt(32)
+    for causal in (False, True):
+        o_ref, lse_ref, _ = A.forward_head(Q, K, V, tau, causal)
+        for i in range(100):
+            x = tau * (K @ Q[i])
+            n_vis = i + 1 if causal else 100
+            bounds = [(j, min(j + 16, n_vis)) for j in range(0, n_vis, 16)]
+            m, l, o, _ = A.online_softmax(x, V, bounds)
+            assert np.abs(o / l - o_ref[i]).max() < 1e-12
+            assert abs(m + math.log(l) - lse_ref[i]) < 1e-12
+
+
+def test_huge_scores_do_not_overflow():
+    """Lesson4 §2: the naive e^x overflows past 89 in fp32; the safe and online forms do not."""
+    x = np.array([1000.0, 999.0, 10.0, 1001.0])
+    v = np.array([[1.0], [2.0], [3.0], [4.0]])
+    p, m, l = A.three_pass_softmax(x[None, :])
+    assert np.isfinite(p).all() and m[0] == 1001.0
+    mo, lo, oo, _ = A.online_softmax(x, v, [(0, 1), (1, 3), (3, 4)])
+    np.testing.assert_allclose(oo / lo, (p @ v)[0], atol=1e-13)
+
+
+# ---------------------------------------------------------------------------------------------
+# Forward: independent library routines and invariants
+# ---------------------------------------------------------------------------------------------
+
+def _sdpa64(q, k, v, scale, causal):
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))
+    o = torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v), is_causal=causal,
+                                                         scale=scale)
+    return o.numpy()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", [(2, 3, 37, 37, 16), (1, 2, 130, 130, 64), (1, 1, 5, 9, 8)])
+def test_forward_vs_torch_sdpa_fp64(shape, causal):
+    B, H, nq, nkv, d = shape
+    if causal and nq != nkv:
+        pytest.skip("causal is defined for N_q == N_kv")
+    q, k, v, _ = rng_inputs(7, B, H, nq, nkv, d)
+    tau = 1 / math.sqrt(d)
+    o, lse = A.forward(q, k, v, tau, causal)
+    np.testing.assert_allclose(o, _sdpa64(q, k, v, tau, causal), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_vs_scipy_softmax_logsumexp(causal):
+    from scipy.special import logsumexp, softmax
+    q, k, v, _ = rng_inputs(3, 1, 2, 50, 50, 12)
+    tau = 0.37
+    o, lse = A.forward(q, k, v, tau, causal)
+    for h in range(2):
+        s = tau * q[0, h] @ k[0, h].T
+        if causal:
+            s = s + np.triu(np.full((50, 50), -np.inf), 1)
+        np.testing.assert_allclose(lse[0, h], logsumexp(s, axis=1), atol=1e-12)
+        np.testing.assert_allclose(o[0, h], softmax(s, axis=1) @ v[0, h], atol=1e-12)
+
+
+def test_rows_of_p_sum_to_one():
+    q, k, v, _ = rng_inputs(5, 1, 1, 64, 80, 16)
+    for causal in (False,):
+        _, _, p = A.forward_head(q[0, 0], k[0, 0], v[0, 0], 0.25, causal)
+        np.testing.assert_allclose(p.sum(axis=1), 1.0, atol=1e-14)
+    q, k, v, _ = rng_inputs(6, 1, 1, 64, 64, 16)
+    _, _, p = A.forward_head(q[0, 0], k[0, 0], v[0, 0], 0.25, True)
+    np.testing.assert_allclose(p.sum(axis=1), 1.0, atol=1e-14)
+    assert (np.triu(p, 1) == 0).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_constant_v_gives_o_equal_v(causal):
+    q, k, _, _ = rng_inputs(8, 1, 2, 40, 40, 8)
+    row = np.arange(8.0) - 3.5
+    v = np.broadcast_to(row, (1, 2, 40, 8)).copy()
+    o, _ = A.forward(q, k, v, 0.5, causal)
+    np.testing.assert_allclose(o, v[:, :, :40], atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_query_is_uniform_average(causal):
+    _, k, v, _ = rng_inputs(9, 1, 1, 30, 30, 6)
+    q = np.zeros((1, 1, 30, 6))
+    o, lse = A.forward(q, k, v, 1.0, causal)
+    for i in range(30):
+        n = i + 1 if causal else 30
+        np.testing.assert_allclose(o[0, 0, i], v[0, 0, :n].mean(axis=0), atol=1e-13)
+        assert abs(lse[0, 0, i] - math.log(n)) < 1e-13
+
+
+def test_identical_keys_uniform_and_shifted_lse():
+    q, _, v, _ = rng_inputs(10, 1, 1, 12, 20, 4)
+    k1 = np.random.default_rng(1).standard_normal(4)
+    k = np.broadcast_to(k1, (1, 1, 20, 4)).copy()
+    tau = 0.3
+    o, lse = A.forward(q, k, v, tau, False)
+    for i in range(12):
+        np.testing.assert_allclose(o[0, 0, i], v[0, 0].mean(axis=0), atol=1e-13)
+        assert abs(lse[0, 0, i] - (tau * q[0, 0, i] @ k1 + math.log(20))) < 1e-12
+
+
+def test_causal_row0_sees_only_key0():
+    q, k, v, _ = rng_inputs(11, 1, 1, 16, 16, 8)
+    tau = 0.2
+    o, lse = A.forward(q, k, v, tau, True)
+    np.testing.assert_allclose(o[0, 0, 0], v[0, 0, 0], atol=1e-15)
+    assert abs(lse[0, 0, 0] - tau * q[0, 0, 0] @ k[0, 0, 0]) < 1e-14
+
+
+def test_empty_key_set():
+    q = np.ones((1, 1, 3, 4))
+    k = np.zeros((1, 1, 0, 4))
+    v = np.zeros((1, 1, 0, 4))
+    o, lse = A.forward(q, k, v, 1.0, False)
+    assert (o == 0).all() and np.isneginf(lse).all()
+    o, lse = A.merge(np.zeros(2), -np.inf, np.zeros(2), -np.inf)
+    assert (o == 0).all() and lse == -np.inf
+    o, lse = A.merge(np.array([1.0, 2.0]), 0.5, np.zeros(2), -np.inf)
+    assert (o == [1.0, 2.0]).all() and lse == 0.5
+
+
+def test_forward_rows_matches_full_head():
+    q, k, v, _ = rng_inputs(12, 1, 1, 70, 70, 8)
+    o, lse, _ = A.forward_head(q[0, 0], k[0, 0], v[0, 0], 0.4, True)
+    idx = np.array([0, 5, 33, 69])
+    o2, lse2 = A.forward_rows(q[0, 0, idx], idx, k[0, 0], v[0, 0], 0.4, True)
+    np.testing.assert_allclose(o2, o[idx], atol=1e-15)
+    np.testing.assert_allclose(lse2, lse[idx], atol=1e-15)
+
+
+# ---------------------------------------------------------------------------------------------
+# Backward: finite differences, torch autograd, the D identity
+# ---------------------------------------------------------------------------------------------
+
+def _loss(q, k, v, do, tau, causal):
+    o, _ = A.forward(q, k, v, tau, causal)
+    return float((do * o).sum())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", [(1, 1, 5, 5, 3), (1, 2, 8, 8, 4), (1, 1, 3, 7, 2)])
+def test_backward_central_finite_differences(shape, causal):
+    B, H, nq, nkv, d = shape
+    if causal and nq != nkv:
+        pytest.skip("causal is defined for N_q == N_kv")
+    q, k, v, do = rng_inputs(13, B, H, nq, nkv, d)
+    tau = 0.7
+    dq, dk, dv, _ = A.backward(q, k, v, do, tau, causal)
+    h = 1e-6
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        it = np.nditer(x, flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            old = x[idx]
+            x[idx] = old + h
+            lp = _loss(q, k, v, do, tau, causal)
+            x[idx] = old - h
+            lm = _loss(q, k, v, do, tau, causal)
+            x[idx] = old
+            num[idx] = (lp - lm) / (2 * h)
+        scale = max(1.0, np.abs(g).max())
+        assert np.abs(num - g).max() / scale < 1e-7
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_vs_torch_autograd_fp64(causal):
+    q, k, v, do = rng_inputs(14, 2, 2, 48, 48, 16)
+    tau = 0.25
+    dq, dk, dv, _ = A.backward(q, k, v, do, tau, causal)
+    tq, tk, tv = (torch.from_numpy(a.copy()).requires_grad_() for a in (q, k, v))
+    s = tau * tq @ tk.transpose(-1, -2)
+    if causal:
+        s = s.masked_fill(torch.ones(48, 48, dtype=torch.bool).triu(1), float("-inf"))
+    o = torch.softmax(s, dim=-1) @ tv
+    o.backward(torch.from_numpy(do))
+    np.testing.assert_allclose(dq, tq.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dk, tk.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-12)
+
+
+def test_D_identity_rowsum_do_o():
+    """Lesson4 §3 'Backward pass', step 3: D_i = sum_j P_ij dP_ij = dO_i . O_i."""
+    q, k, v, do = rng_inputs(15, 1, 3, 33, 33, 8)
+    for causal in (False, True):
+        o, _ = A.forward(q, k, v, 0.3, causal)
+        _, _, _, D = A.backward(q, k, v, do, 0.3, causal)
+        np.testing.assert_allclose(D, (do * o).sum(axis=-1), atol=1e-13)
+
+
+# ---------------------------------------------------------------------------------------------
+# Split-KV decode
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n_kv,n_splits", [(512, 8), (1000, 7), (37, 64), (64, 1), (5, 5)])
+def test_decode_partials_merge_equals_full_row(n_kv, n_splits):
+    q, k, v, _ = rng_inputs(16, 1, 1, 1, n_kv, 16)
+    tau = 0.25
+    m, l, o = A.decode_partials(q[0, 0], k[0, 0], v[0, 0], tau, n_splits)
+    out, lse = A.decode_merge(m, l, o)
+    o_ref, lse_ref = A.decode(q, k, v, tau)
+    np.testing.assert_allclose(out, o_ref[0, 0, 0], atol=1e-13)
+    assert abs(lse - lse_ref[0, 0, 0]) < 1e-12
+    # the same result by folding the pairwise (o, lse) merge over the chunks
+    acc_o, acc_lse = np.zeros(16), -np.inf
+    for c in range(n_splits):
+        if np.isfinite(m[c]):
+            acc_o, acc_lse = A.merge(acc_o, acc_lse, o[c] / l[c], m[c] + math.log(l[c]))
+        else:
+            acc_o, acc_lse = A.merge(acc_o, acc_lse, np.zeros(16), -np.inf)
+    np.testing.assert_allclose(acc_o, o_ref[0, 0, 0], atol=1e-13)
+
+
+def test_merge_is_associative_and_order_free():
+    g = np.random.default_rng(17)
+    parts = [(g.standard_normal(3), float(g.standard_normal() * 5)) for _ in range(5)]
+    def fold(seq):
+        o, lse = np.zeros(3), -np.inf
+        for po, pl in seq:
+            o, lse = A.merge(o, lse, po, pl)
+        return o, lse
+    o1, l1 = fold(parts)
+    o2, l2 = fold(parts[::-1])
+    np.testing.assert_allclose(o1, o2, atol=1e-14)
+    assert abs(l1 - l2) < 1e-13
+    w = np.exp(np.array([p[1] for p in parts]) - l1)
+    assert abs(w.sum() - 1) < 1e-14                     # merge weights sum to 1
