@@ -1,0 +1,218 @@
+"""exact_io_aware_08_gb300 -- exact IO-aware attention (FlashAttention) for GB300 (sm_103a).
+
+A thin ctypes binding over ``libfa.so`` (the C ABI in ``include/fa.h``).  Functions with the C
+names take torch CUDA tensors and only marshal pointers, sizes and the current stream; every
+step of the computation runs in the library's kernels.  There is no fallback: if the library is
+missing or a call is rejected, a ``FaError`` is raised.
+
+Convenience wrappers ``forward``, ``backward`` and ``decode`` allocate outputs with torch (the
+library itself never allocates).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "FaError", "load_library", "library_path",
+    "fa_fwd", "fa_bwd", "fa_bwd_prep", "fa_bwd_main", "fa_bwd_finish", "fa_decode_splitkv", "fa_bwd_workspace_size",
+    "fa_decode_workspace_size", "fa_sync_status", "fa_status_string", "fa_last_error_message",
+    "forward", "backward", "decode",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libfa.so")
+_lib = None
+_lock = threading.Lock()
+
+FA_OK = 0
+STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_WORKSPACE",
+                4: "FA_ERR_CUDA", 5: "FA_ERR_DEVICE_TIMEOUT"}
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_S = ctypes.c_size_t
+
+_SIGNATURES = {
+    "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_bwd_workspace_size": (_S, [_I, _I, _I, _I, _I]),
+    "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_bwd_prep": (_I, [_P, _P, _P, _S, _I, _I, _I, _I, _I, _P]),
+    "fa_bwd_main": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_bwd_finish": (_I, [_P, _P, _S, _I, _I, _I, _I, _I, _F, _P]),
+    "fa_decode_workspace_size": (_S, [_I, _I, _I, _I, _I]),
+    "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
+    "fa_sync_status": (_I, [_P]),
+    "fa_status_string": (ctypes.c_char_p, [_I]),
+    "fa_last_error_message": (ctypes.c_char_p, []),
+}
+
+
+def load_library(path: str | None = None):
+    """Load libfa.so (raises FaError if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _LIB_PATH
+        if not os.path.exists(p):
+            raise FaError(4, f"{p} not found: build it with `python -m exact_io_aware_08_gb300.build`"
+                             " (the library has no fallback implementation)")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != FA_OK:
+        lib = load_library()
+        raise FaError(status, lib.fa_last_error_message().decode())
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _dims(q, k):
+    B, H, n_q, d = q.shape
+    return B, H, n_q, k.shape[2], d
+
+
+# --------------------------------------------------------------------------------------------
+# C-named entry points (pointers from tensors; no allocation, no computation)
+# --------------------------------------------------------------------------------------------
+
+def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None):
+    B, H, n_q, n_kv, d = _dims(q, k)
+    _check(load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, n_q, n_kv,
+                                 d, float(scale), int(bool(causal)), _stream(stream)))
+
+
+def fa_bwd_workspace_size(B: int, H: int, n_q: int, n_kv: int, d: int) -> int:
+    return int(load_library().fa_bwd_workspace_size(B, H, n_q, n_kv, d))
+
+
+def fa_bwd(q, k, v, o, lse, do, dq, dk, dv, ws, scale: float, causal: bool, stream=None):
+    B, H, n_q, n_kv, d = _dims(q, k)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq),
+                                 _ptr(dk), _ptr(dv), _ptr(ws), ws_bytes, B, H, n_q, n_kv, d,
+                                 float(scale), int(bool(causal)), _stream(stream)))
+
+
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def fa_bwd_prep(o, do, ws, n_kv: int, stream=None):
+    B, H, n_q, d = o.shape
+    _check(load_library().fa_bwd_prep(_ptr(o), _ptr(do), _ptr(ws), _nbytes(ws), B, H, n_q, n_kv, d,
+                                      _stream(stream)))
+
+
+def fa_bwd_main(q, k, v, lse, do, dk, dv, ws, scale: float, causal: bool, stream=None):
+    B, H, n_q, n_kv, d = _dims(q, k)
+    _check(load_library().fa_bwd_main(_ptr(q), _ptr(k), _ptr(v), _ptr(lse), _ptr(do), _ptr(dk),
+                                      _ptr(dv), _ptr(ws), _nbytes(ws), B, H, n_q, n_kv, d,
+                                      float(scale), int(bool(causal)), _stream(stream)))
+
+
+def fa_bwd_finish(dq, ws, n_kv: int, scale: float, stream=None):
+    B, H, n_q, d = dq.shape
+    _check(load_library().fa_bwd_finish(_ptr(dq), _ptr(ws), _nbytes(ws), B, H, n_q, n_kv, d,
+                                        float(scale), _stream(stream)))
+
+
+def fa_decode_workspace_size(B: int, H: int, n_kv: int, d: int, n_splits: int) -> int:
+    return int(load_library().fa_decode_workspace_size(B, H, n_kv, d, n_splits))
+
+
+def fa_decode_splitkv(q, k, v, o, lse, scale: float, n_splits: int, ws, stream=None):
+    B, H, _, d = q.shape
+    n_kv = k.shape[2]
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load_library().fa_decode_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, n_kv,
+                                            d, float(scale), int(n_splits), _ptr(ws), ws_bytes,
+                                            _stream(stream)))
+
+
+def fa_sync_status(stream=None):
+    _check(load_library().fa_sync_status(_stream(stream)))
+
+
+def fa_status_string(status: int) -> str:
+    return load_library().fa_status_string(status).decode()
+
+
+def fa_last_error_message() -> str:
+    return load_library().fa_last_error_message().decode()
+
+
+# --------------------------------------------------------------------------------------------
+# Convenience wrappers: torch allocates the outputs, the library computes them
+# --------------------------------------------------------------------------------------------
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=None):
+    """Returns (O bf16 [B,H,N_q,d], lse fp32 [B,H,N_q])."""
+    import torch
+    d = q.shape[-1]
+    scale = d ** -0.5 if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    fa_fwd(q, k, v, o, lse, scale, causal, stream)
+    return o, lse
+
+
+def backward(q, k, v, o, lse, do, causal: bool = False, scale: float | None = None, stream=None,
+             workspace=None):
+    """Returns (dQ, dK, dV) in bf16."""
+    import torch
+    B, H, n_q, d = q.shape
+    scale = d ** -0.5 if scale is None else scale
+    need = fa_bwd_workspace_size(B, H, n_q, k.shape[2], d)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    fa_bwd(q, k, v, o, lse, do, dq, dk, dv, workspace, scale, causal, stream)
+    return dq, dk, dv
+
+
+def decode(q, k, v, n_splits: int = 0, scale: float | None = None, stream=None, workspace=None):
+    """Single-query split-KV decode: q [B,H,1,d], k/v [B,H,N_kv,d] -> (O [B,H,1,d], lse [B,H,1])."""
+    import torch
+    B, H, _, d = q.shape
+    scale = d ** -0.5 if scale is None else scale
+    need = fa_decode_workspace_size(B, H, k.shape[2], d, n_splits)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, 1), dtype=torch.float32, device=q.device)
+    fa_decode_splitkv(q, k, v, o, lse, scale, n_splits, workspace, stream)
+    return o, lse

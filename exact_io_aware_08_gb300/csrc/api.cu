@@ -1,0 +1,236 @@
+// C ABI of libfa (declared in include/fa.h): argument validation, workspace carving, dispatch
+// to the kernel launchers, device-status collection.  Nothing here allocates memory or falls
+// back to another implementation: an unsupported call returns an error before any launch.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/fa.h"
+#include "fa_kernels.h"
+
+namespace {
+
+thread_local char g_msg[512] = "no error";
+
+fa_status_t fail(fa_status_t st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+fa_status_t cuda_fail(cudaError_t e, const char* what) {
+  return fail(FA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shared shape checks.  Returns FA_OK or an error (message set).
+fa_status_t check_shape(int B, int H, int n_q, int n_kv, int d, float scale) {
+  if (B < 1 || H < 1) return fail(FA_ERR_INVALID_ARG, "B and H must be >= 1 (got B=%d H=%d)", B, H);
+  if (n_q < 0 || n_kv < 0)
+    return fail(FA_ERR_INVALID_ARG, "sequence lengths must be >= 0 (got N_q=%d N_kv=%d)", n_q, n_kv);
+  if (d != 64 && d != 128) return fail(FA_ERR_UNSUPPORTED, "head dim d=%d not supported (64 or 128)", d);
+  if (!std::isfinite(scale) || !(scale > 0.f))
+    return fail(FA_ERR_INVALID_ARG, "scale must be finite and > 0 (got %g)", static_cast<double>(scale));
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > (1LL << 30)) return fail(FA_ERR_UNSUPPORTED, "B*H=%lld too large", bh);
+  const long long lim = (1LL << 31) / d;
+  if (n_q >= lim || n_kv >= lim)
+    return fail(FA_ERR_UNSUPPORTED, "sequence length too large for d=%d (limit %lld)", d, lim);
+  // grid of (query tiles x heads) must fit in gridDim.x
+  const long long tiles = (static_cast<long long>(n_q) + 127) / 128;
+  if (tiles * bh >= (1LL << 31)) return fail(FA_ERR_UNSUPPORTED, "too many (tile, head) work items");
+  return FA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_status_string(fa_status_t s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT";
+  }
+  return "FA_ERR_UNKNOWN";
+}
+
+const char* fa_last_error_message(void) { return g_msg; }
+
+fa_status_t fa_fwd(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v, fa_bf16_t* o,
+                   float* lse, int B, int H, int N_q, int N_kv, int d, float scale, int causal,
+                   void* stream) {
+  fa_status_t st = check_shape(B, H, N_q, N_kv, d, scale);
+  if (st != FA_OK) return st;
+  if (causal && N_q != N_kv)
+    return fail(FA_ERR_UNSUPPORTED, "causal requires N_q == N_kv (got %d, %d)", N_q, N_kv);
+  if (N_q == 0) return FA_OK;
+  if (!q || !o || !lse || (N_kv > 0 && (!k || !v)))
+    return fail(FA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(FA_ERR_INVALID_ARG, "arrays must be 16-byte aligned");
+  fa::FwdArgs a{q, k ? k : q, v ? v : q, o, lse, B, H, N_q, N_kv, d, scale, causal ? 1 : 0};
+  if (N_kv == 0) { a.k = q; a.v = q; }   // maps need a valid base; no key tile is read
+  cudaError_t e = fa::launch_fwd(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_fwd launch");
+  return FA_OK;
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N_q, int N_kv, int d) {
+  if (B < 1 || H < 1 || N_q < 0 || N_kv < 0 || (d != 64 && d != 128)) return 0;
+  return fa::bwd_dq_acc_bytes(B, H, N_q, d) + fa::bwd_delta_bytes(B, H, N_q);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Validation shared by fa_bwd and its three steps.  ``need`` selects which arrays must be
+// present: bit i for argument i of {q, k, v, o, lse, dO, dq, dk, dv}.
+fa_status_t check_bwd(const void* const (&ptrs)[9], unsigned need, const void* ws, size_t ws_bytes,
+                      int B, int H, int N_q, int N_kv, int d, float scale, int causal,
+                      fa::BwdArgs* a) {
+  fa_status_t st = check_shape(B, H, N_q, N_kv, d, scale);
+  if (st != FA_OK) return st;
+  if (causal && N_q != N_kv)
+    return fail(FA_ERR_UNSUPPORTED, "causal requires N_q == N_kv (got %d, %d)", N_q, N_kv);
+  const bool rows_q[9] = {true, false, false, true, true, true, true, false, false};
+  for (int i = 0; i < 9; ++i) {
+    const bool nonempty = rows_q[i] ? N_q > 0 : N_kv > 0;
+    if ((need >> i & 1u) && nonempty && !ptrs[i])
+      return fail(FA_ERR_INVALID_ARG, "null pointer argument (#%d)", i);
+    if (ptrs[i] && !aligned16(ptrs[i])) return fail(FA_ERR_INVALID_ARG, "arrays must be 16-byte aligned");
+  }
+  const size_t need_ws = fa_bwd_workspace_size(B, H, N_q, N_kv, d);
+  if (!ws || ws_bytes < need_ws || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return fail(FA_ERR_WORKSPACE, "workspace must be >= %zu bytes and 256-byte aligned (got %zu)",
+                need_ws, ws_bytes);
+  *a = fa::BwdArgs{};
+  a->q = ptrs[0]; a->k = ptrs[1]; a->v = ptrs[2]; a->o = ptrs[3];
+  a->lse = static_cast<const float*>(ptrs[4]); a->dO = ptrs[5];
+  a->dq = const_cast<void*>(ptrs[6]); a->dk = const_cast<void*>(ptrs[7]);
+  a->dv = const_cast<void*>(ptrs[8]);
+  a->dq_acc = static_cast<float*>(const_cast<void*>(ws));
+  a->delta = reinterpret_cast<float*>(static_cast<char*>(const_cast<void*>(ws)) +
+                                      fa::bwd_dq_acc_bytes(B, H, N_q, d));
+  a->B = B; a->H = H; a->n_q = N_q; a->n_kv = N_kv; a->d = d; a->scale = scale;
+  a->causal = causal ? 1 : 0;
+  return FA_OK;
+}
+
+constexpr unsigned kNeedAll = 0x1FFu;
+constexpr unsigned kNeedPrep = (1u << 3) | (1u << 5);                                  // o, dO
+constexpr unsigned kNeedMain = 1u | 2u | 4u | (1u << 4) | (1u << 5) | (1u << 7) | (1u << 8);
+constexpr unsigned kNeedFinish = 1u << 6;                                              // dq
+
+}  // namespace
+
+extern "C" {
+
+fa_status_t fa_bwd(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
+                   const fa_bf16_t* o, const float* lse, const fa_bf16_t* dO, fa_bf16_t* dq,
+                   fa_bf16_t* dk, fa_bf16_t* dv, void* ws, size_t ws_bytes, int B, int H,
+                   int N_q, int N_kv, int d, float scale, int causal, void* stream) {
+  fa::BwdArgs a;
+  const void* const ptrs[9] = {q, k, v, o, lse, dO, dq, dk, dv};
+  fa_status_t st = check_bwd(ptrs, kNeedAll, ws, ws_bytes, B, H, N_q, N_kv, d, scale, causal, &a);
+  if (st != FA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = fa::launch_bwd_prep(a, s);
+  if (e == cudaSuccess) e = fa::launch_bwd_main(a, s);
+  if (e == cudaSuccess) e = fa::launch_bwd_finish(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_bwd launch");
+  return FA_OK;
+}
+
+fa_status_t fa_bwd_prep(const fa_bf16_t* o, const fa_bf16_t* dO, void* ws, size_t ws_bytes,
+                        int B, int H, int N_q, int N_kv, int d, void* stream) {
+  fa::BwdArgs a;
+  const void* const ptrs[9] = {nullptr, nullptr, nullptr, o, nullptr, dO, nullptr, nullptr, nullptr};
+  fa_status_t st = check_bwd(ptrs, kNeedPrep, ws, ws_bytes, B, H, N_q, N_kv, d, 1.f, 0, &a);
+  if (st != FA_OK) return st;
+  cudaError_t e = fa::launch_bwd_prep(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e, "fa_bwd_prep launch");
+}
+
+fa_status_t fa_bwd_main(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
+                        const float* lse, const fa_bf16_t* dO, fa_bf16_t* dk, fa_bf16_t* dv,
+                        void* ws, size_t ws_bytes, int B, int H, int N_q, int N_kv, int d,
+                        float scale, int causal, void* stream) {
+  fa::BwdArgs a;
+  const void* const ptrs[9] = {q, k, v, nullptr, lse, dO, nullptr, dk, dv};
+  fa_status_t st = check_bwd(ptrs, kNeedMain, ws, ws_bytes, B, H, N_q, N_kv, d, scale, causal, &a);
+  if (st != FA_OK) return st;
+  cudaError_t e = fa::launch_bwd_main(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e, "fa_bwd_main launch");
+}
+
+fa_status_t fa_bwd_finish(fa_bf16_t* dq, const void* ws, size_t ws_bytes, int B, int H, int N_q,
+                          int N_kv, int d, float scale, void* stream) {
+  fa::BwdArgs a;
+  const void* const ptrs[9] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, dq, nullptr, nullptr};
+  fa_status_t st = check_bwd(ptrs, kNeedFinish, ws, ws_bytes, B, H, N_q, N_kv, d, scale, 0, &a);
+  if (st != FA_OK) return st;
+  cudaError_t e = fa::launch_bwd_finish(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FA_OK : cuda_fail(e, "fa_bwd_finish launch");
+}
+
+size_t fa_decode_workspace_size(int B, int H, int N_kv, int d, int n_splits) {
+  if (B < 1 || H < 1 || N_kv < 0 || (d != 64 && d != 128)) return 0;
+  if (n_splits <= 0) n_splits = fa::decode_auto_splits(B, H, N_kv);
+  if (n_splits > fa::kDecodeMaxSplits) return 0;
+  return fa::decode_part_bytes(B, H, d, n_splits);
+}
+
+fa_status_t fa_decode_splitkv(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
+                              fa_bf16_t* o, float* lse, int B, int H, int N_kv, int d,
+                              float scale, int n_splits, void* ws, size_t ws_bytes,
+                              void* stream) {
+  fa_status_t st = check_shape(B, H, 1, N_kv, d, scale);
+  if (st != FA_OK) return st;
+  if (n_splits > fa::kDecodeMaxSplits)
+    return fail(FA_ERR_UNSUPPORTED, "n_splits=%d exceeds %d", n_splits, fa::kDecodeMaxSplits);
+  if (n_splits <= 0) n_splits = fa::decode_auto_splits(B, H, N_kv);
+  if (!q || !o || !lse || (N_kv > 0 && (!k || !v)))
+    return fail(FA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(FA_ERR_INVALID_ARG, "arrays must be 16-byte aligned");
+  const size_t need_ws = fa::decode_part_bytes(B, H, d, n_splits);
+  if (!ws || ws_bytes < need_ws || !aligned16(ws))
+    return fail(FA_ERR_WORKSPACE, "workspace must be >= %zu bytes and 16-byte aligned (got %zu)",
+                need_ws, ws_bytes);
+  fa::DecodeArgs a{};
+  a.q = q; a.k = N_kv ? k : q; a.v = N_kv ? v : q; a.o = o; a.lse = lse;
+  a.part = static_cast<float*>(ws);
+  a.B = B; a.H = H; a.n_kv = N_kv; a.d = d; a.scale = scale; a.n_splits = n_splits;
+  a.chunk = fa::decode_chunk(N_kv, n_splits);
+  cudaError_t e = fa::launch_decode(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_decode_splitkv launch");
+  return FA_OK;
+}
+
+fa_status_t fa_sync_status(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned int code = 0, c = 0;
+  int where = 0, w = 0;
+  cudaError_t (*fetch[])(cudaStream_t, unsigned int*, int*) = {
+      fa::status_fetch_fwd, fa::status_fetch_bwd, fa::status_fetch_decode};
+  for (auto f : fetch) {
+    cudaError_t e = f(s, &c, &w);
+    if (e != cudaSuccess) return cuda_fail(e, "fa_sync_status");
+    if (c) { code |= c; where = w; }
+  }
+  if (code & fa::FA_DEV_TIMEOUT)
+    return fail(FA_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait ran out (site %d)", where);
+  if (code) return fail(FA_ERR_CUDA, "device reported error code %u (site %d)", code, where);
+  return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,116 @@
+// Internal launcher interface between the C ABI (api.cu) and the kernel translation units.
+// Arguments arrive here already validated.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "host_tma.h"
+
+namespace fa {
+
+// Codes kernels record in their translation unit's device status word.
+enum DevError : unsigned int {
+  FA_DEV_TIMEOUT = 1u,       // a bounded mbarrier wait ran out
+  FA_DEV_BAD_CONFIG = 2u,    // kernel found launch geometry it was not built for
+};
+
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B, H, n_q, n_kv, d;
+  float scale;
+  int causal;
+};
+
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const float* lse;
+  const void* dO;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* dq_acc;     // fp32 [B,H,N_q,d] workspace
+  float* delta;      // fp32 [B,H,N_q]   workspace (D = rowsum(dO o O))
+  int B, H, n_q, n_kv, d;
+  float scale;
+  int causal;
+};
+
+struct DecodeArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  float* part;       // fp32 [B*H, n_splits, d + 2]: (o~[d], m, l) per chunk
+  int B, H, n_kv, d;
+  float scale;
+  int n_splits;
+  int chunk;         // keys per split (multiple of the kernel's key step)
+};
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t stream);    // F2
+cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream);    // F3
+cudaError_t launch_bwd_finish(const BwdArgs& a, cudaStream_t stream);  // F4
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// Per-TU device status accessors (see fa_status.cuh).
+cudaError_t status_fetch_fwd(cudaStream_t, unsigned int*, int*);
+cudaError_t status_fetch_bwd(cudaStream_t, unsigned int*, int*);
+cudaError_t status_fetch_decode(cudaStream_t, unsigned int*, int*);
+
+// Workspace layout of the backward pass.
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline size_t bwd_dq_acc_bytes(int B, int H, int n_q, int d) {
+  return align_up(static_cast<size_t>(B) * H * n_q * d * sizeof(float), 256);
+}
+inline size_t bwd_delta_bytes(int B, int H, int n_q) {
+  return align_up(static_cast<size_t>(B) * H * n_q * sizeof(float), 256);
+}
+
+// Decode split policy: keys per chunk are a multiple of 64; n_splits <= 0 picks a count that
+// gives every SM several CTAs when B*H alone does not.
+constexpr int kDecodeKeyStep = 64;
+constexpr int kDecodeMaxSplits = 1024;
+inline int decode_auto_splits(int B, int H, int n_kv) {
+  const long long bh = static_cast<long long>(B) * H;
+  const long long want_ctas = 152LL * 8;
+  long long s = (want_ctas + bh - 1) / bh;
+  const long long max_by_len = (n_kv + 255) / 256;       // at least ~256 keys per chunk
+  if (s > max_by_len) s = max_by_len;
+  if (s < 1) s = 1;
+  if (s > kDecodeMaxSplits) s = kDecodeMaxSplits;
+  return static_cast<int>(s);
+}
+inline int decode_chunk(int n_kv, int n_splits) {
+  int c = (n_kv + n_splits - 1) / n_splits;
+  c = (c + kDecodeKeyStep - 1) / kDecodeKeyStep * kDecodeKeyStep;
+  return c < kDecodeKeyStep ? kDecodeKeyStep : c;
+}
+inline size_t decode_part_bytes(int B, int H, int d, int n_splits) {
+  return static_cast<size_t>(B) * H * n_splits * (d + 2) * sizeof(float);
+}
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (kernel, device).  ``done`` is a
+// per-kernel flag array owned by the caller (kernels of the same signature must not share one).
+template <typename F>
+cudaError_t ensure_smem_attr(F* func, int bytes, int (&done)[64]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && __atomic_load_n(&done[dev], __ATOMIC_ACQUIRE)) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev < 64) __atomic_store_n(&done[dev], 1, __ATOMIC_RELEASE);
+  return e;
+}
+
+}  // namespace fa

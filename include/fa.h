@@ -1,0 +1,157 @@
+/*
+ * fa.h -- C ABI of libfa: exact IO-aware attention (FlashAttention forward, backward and
+ * split-KV decode) for NVIDIA GB300 (sm_103a).
+ *
+ * Pages this interface follows (cited by title and section):
+ *   [Lesson4]  "FlashAttention and online softmax", ML Systems lesson 4.
+ *   [Scratch]  "FlashAttention from Scratch -- The Paradox of Doing More Math to Go Faster".
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  Layout     q, k, v, o, dO, dq, dk, dv are dense row-major [B, H, N, d] arrays of bfloat16
+ *             (raw 16-bit patterns, type fa_bf16_t), d fastest.  lse is fp32 [B, H, N_q],
+ *             natural logarithm.  Shapes (batch, heads, N, d) as in [Lesson4] section 5.
+ *  Pointers   All array pointers are DEVICE pointers owned by the caller.  The library never
+ *             allocates, frees or keeps a pointer after the call returns.  Every array must be
+ *             16-byte aligned (TMA requirement).
+ *  Streams    ``stream`` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *             Calls only enqueue work and return; nothing synchronises except fa_sync_status.
+ *  Support    d in {64, 128}; 1 <= B*H; N_q, N_kv >= 0 and < 2^31 / d.  ``causal`` means query i
+ *             sees keys j <= i ([Lesson4] "Causal masks") and requires N_q == N_kv.
+ *  Errors     Argument problems are reported by the return value BEFORE anything is launched;
+ *             there is no fallback path (a silent fallback is the failure mode [Scratch] "How
+ *             this shows up in practice" warns about).  Device-side bounded waits that run out
+ *             are reported later by fa_sync_status.  fa_last_error_message() gives a one-line
+ *             description of the last failure on the calling thread.
+ *  Empty      N_kv == 0 gives O = 0 and lse = -inf; N_q == 0 does nothing
+ *             ([Lesson4] section 3 "Compute it stably": an empty set has lse = -inf).
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t fa_bf16_t; /* raw bfloat16 bits */
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,    /* null pointer, negative size, misaligned pointer, bad scale */
+  FA_ERR_UNSUPPORTED = 2,    /* d not in {64,128}; causal with N_q != N_kv; size limits */
+  FA_ERR_WORKSPACE = 3,      /* workspace pointer null or smaller than the *_workspace_size */
+  FA_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed (message has the detail) */
+  FA_ERR_DEVICE_TIMEOUT = 5  /* a kernel's bounded wait ran out; its outputs are invalid */
+} fa_status_t;
+
+/*
+ * fa_fwd -- attention forward pass.  [Lesson4] section 3 "The tiled forward pass" and
+ * "The online softmax theorem"; [Scratch] "Online softmax: shrink the running total".
+ *
+ *   O   = softmax(scale * Q K^T (+ causal mask)) V         bf16 [B, H, N_q, d]
+ *   lse = m + log(l) per query row (natural log)           fp32 [B, H, N_q]
+ *
+ * Tiles of 128 query rows stay on chip while 128-key tiles of K and V stream through shared
+ * memory; the N_q x N_kv score matrix is never written to memory.
+ * q: [B,H,N_q,d]; k, v: [B,H,N_kv,d]; o: [B,H,N_q,d] (written); lse: [B,H,N_q] (written).
+ * scale must be finite and > 0 (normally 1/sqrt(d)).
+ */
+fa_status_t fa_fwd(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v, fa_bf16_t* o,
+                   float* lse, int B, int H, int N_q, int N_kv, int d, float scale, int causal,
+                   void* stream);
+
+/*
+ * Workspace bytes fa_bwd needs: an fp32 dQ accumulator [B,H,N_q,d] plus fp32 D [B,H,N_q]
+ * plus alignment padding.  Returns 0 for unsupported arguments.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N_q, int N_kv, int d);
+
+/*
+ * fa_bwd -- recompute-based backward pass.  [Lesson4] section 3 "Backward pass: recompute
+ * instead of store", steps 1-4; [Scratch] "Recomputing on purpose in the backward pass".
+ *
+ *   D  = rowsum(dO o O)                     (pre-kernel, fp32, into the workspace)
+ *   P  = exp(scale * Q K^T - lse)           (recomputed tile by tile, never stored)
+ *   dV = P^T dO;  dP = dO V^T;  dS = P o (dP - D)
+ *   dQ = scale * dS K;  dK = scale * dS^T Q
+ *
+ * o and lse must be the outputs of fa_fwd for the same q, k, v, scale and causal.
+ * dq [B,H,N_q,d], dk and dv [B,H,N_kv,d] are written (not accumulated).  ``ws`` is a device
+ * buffer of at least fa_bwd_workspace_size(...) bytes, 256-byte aligned; its contents on entry
+ * are ignored and on exit are unspecified.  dQ is accumulated with fp32 atomics, so dq can
+ * differ between runs in the last bits; dk and dv are deterministic.
+ */
+fa_status_t fa_bwd(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
+                   const fa_bf16_t* o, const float* lse, const fa_bf16_t* dO, fa_bf16_t* dq,
+                   fa_bf16_t* dk, fa_bf16_t* dv, void* ws, size_t ws_bytes, int B, int H,
+                   int N_q, int N_kv, int d, float scale, int causal, void* stream);
+
+/*
+ * The three steps fa_bwd runs, in this order on one stream, exposed so a caller can schedule
+ * or time them separately.  Arguments mean the same as in fa_bwd; the same ``ws`` must be
+ * passed to all three, and only the arrays each step reads or writes are needed (others may
+ * be NULL):
+ *   fa_bwd_prep    D_i = sum_k dO_ik O_ik (fp32, into ws) and clears the fp32 dQ accumulator
+ *                  ([Lesson4] "Backward pass", step 3: D_i = dO_i . O_i).  Reads o, dO.
+ *   fa_bwd_main    recomputes S and P = exp(scale QK^T - lse) per 128-key tile, writes dK and
+ *                  dV, and adds the tile's dS K (not yet multiplied by scale) into the fp32 dQ
+ *                  accumulator (steps 1-4).
+ *                  Reads q, k, v, lse, dO and D; writes dk, dv.
+ *   fa_bwd_finish  dq = bf16(scale * accumulator).  Writes dq.
+ */
+fa_status_t fa_bwd_prep(const fa_bf16_t* o, const fa_bf16_t* dO, void* ws, size_t ws_bytes,
+                        int B, int H, int N_q, int N_kv, int d, void* stream);
+fa_status_t fa_bwd_main(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
+                        const float* lse, const fa_bf16_t* dO, fa_bf16_t* dk, fa_bf16_t* dv,
+                        void* ws, size_t ws_bytes, int B, int H, int N_q, int N_kv, int d,
+                        float scale, int causal, void* stream);
+fa_status_t fa_bwd_finish(fa_bf16_t* dq, const void* ws, size_t ws_bytes, int B, int H, int N_q,
+                          int N_kv, int d, float scale, void* stream);
+
+/*
+ * Workspace bytes fa_decode_splitkv needs for n_splits partial states per (b, h):
+ * fp32 (m, l, o~[d]).  n_splits <= 0 means "automatic" (as fa_decode_splitkv chooses).
+ */
+size_t fa_decode_workspace_size(int B, int H, int N_kv, int d, int n_splits);
+
+/*
+ * fa_decode_splitkv -- single-query decode with the KV axis split into chunks
+ * ([Lesson4] section 3 "Split-KV for decoding (flash-decoding)").
+ *
+ * Each (b, h, chunk) computes its online state (m, l, o~) over c consecutive keys, where
+ * c = ceil(N_kv / n_splits) rounded up to a multiple of 64 (trailing chunks may be empty);
+ * a second kernel merges the states of a row with
+ *   m = max m_c,  l = sum e^{m_c - m} l_c,  O = sum e^{m_c - m} o~_c / l,  lse = m + log l
+ * ([Lesson4] section 3 "Merging two partial results"; empty chunks weigh 0).
+ *
+ * q: [B,H,1,d]; k, v: [B,H,N_kv,d]; o: [B,H,1,d]; lse: [B,H,1].  n_splits in [1, 1024], or
+ * <= 0 for automatic.  ``ws`` holds at least fa_decode_workspace_size(...) bytes, 16-byte
+ * aligned; contents on entry ignored.
+ */
+fa_status_t fa_decode_splitkv(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
+                              fa_bf16_t* o, float* lse, int B, int H, int N_kv, int d,
+                              float scale, int n_splits, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/*
+ * fa_sync_status -- synchronise ``stream`` and report device-side failures recorded by any
+ * kernel of this library since the last call (currently: a bounded pipeline wait that ran
+ * out, FA_ERR_DEVICE_TIMEOUT).  Clears the recorded state.  Also returns FA_ERR_CUDA if the
+ * stream reports an asynchronous CUDA error.
+ */
+fa_status_t fa_sync_status(void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* fa_status_string(fa_status_t status);
+
+/* One-line description of the last non-OK status returned on the calling thread. */
+const char* fa_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -169,6 +169,49 @@ def forward_rows(q_rows, row_index, k, v, scale: float, causal: bool):
     return p @ v, lse_from(m, l)
 
 
+def backward_sampled(q, k, v, do, scale: float, causal: bool, q_rows, k_rows, block: int = 1024):
+    """Gradients of one head at selected rows: dQ at query rows ``q_rows``, dK and dV at key
+    rows ``k_rows`` (for full-size checks where whole N x N matrices do not fit).
+
+    Same definition as ``backward_head``, evaluated for subsets.  Every query row's lse_i and
+    D_i = sum_j P_ij dP_ij is needed; they are formed row by row (rows are independent) in
+    blocks of ``block`` rows.  Then P_ij = e^{S_ij - lse_i} on the needed rows / columns
+    [Lesson4 §3 "Backward pass", step 1: the lse already holds the max and the sum].
+    Returns (dQ [len(q_rows), d], dK [len(k_rows), d], dV [len(k_rows), d]).
+    """
+    q, k, v, do = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(do)
+    n_q = q.shape[0]
+    q_rows = np.asarray(q_rows)
+    k_rows = np.asarray(k_rows)
+    lse = np.empty(n_q)
+    D = np.empty(n_q)
+    for r0 in range(0, n_q, block):
+        rows = np.arange(r0, min(n_q, r0 + block))
+        s = scale * (q[rows] @ k.T)
+        if causal:
+            s = np.where(np.arange(k.shape[0])[None, :] <= rows[:, None], s, NEG_INF)
+        p, m, l = three_pass_softmax(s)
+        lse[rows] = lse_from(m, l)
+        D[rows] = (p * (do[rows] @ v.T)).sum(axis=-1)
+
+    def probs(rows, cols):
+        s = scale * (q[rows] @ k[cols].T)
+        if causal:
+            s = np.where(cols[None, :] <= rows[:, None], s, NEG_INF)
+        return np.exp(s - lse[rows][:, None])
+
+    all_q = np.arange(n_q)
+    all_k = np.arange(k.shape[0])
+    p = probs(q_rows, all_k)
+    ds = p * (do[q_rows] @ v.T - D[q_rows][:, None])
+    dq = scale * (ds @ k)
+    pc = probs(all_q, k_rows)
+    dsc = pc * (do @ v[k_rows].T - D[:, None])
+    dv = pc.T @ do
+    dk = scale * (dsc.T @ q)
+    return dq, dk, dv
+
+
 # --------------------------------------------------------------------------------------------
 # Online recurrence and merge (the method's own steps, pages' notation)
 # --------------------------------------------------------------------------------------------

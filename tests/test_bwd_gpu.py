@@ -1,0 +1,122 @@
+"""Backward pass parity: dQ, dK, dV from the CUDA path (through the C ABI) against the fp64
+oracle.  The GPU backward consumes the GPU forward's own O and lse; the oracle uses its own."""
+import numpy as np
+import pytest
+import torch
+
+import exact_io_aware_08_gb300 as fa
+from exact_io_aware_08_gb300 import inputs
+from oracle import attention as A
+from tests.gpu_common import assert_grad_close, cuda, poisoned, require_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def run_fwd_bwd(x, causal, scale):
+    q, k, v, do = (cuda(x[n]) for n in ("q", "k", "v", "do"))
+    o = poisoned(q.shape, torch.bfloat16)
+    lse = poisoned(q.shape[:3], torch.float32)
+    fa.fa_fwd(q, k, v, o, lse, scale, causal)
+    B, H, nq, d = q.shape
+    ws = torch.full((fa.fa_bwd_workspace_size(B, H, nq, k.shape[2], d),), 255, dtype=torch.uint8,
+                    device="cuda")                       # garbage on entry must not matter
+    dq = poisoned(q.shape, torch.bfloat16)
+    dk = poisoned(k.shape, torch.bfloat16)
+    dv = poisoned(v.shape, torch.bfloat16)
+    fa.fa_bwd(q, k, v, o, lse, do, dq, dk, dv, ws, scale, causal)
+    fa.fa_sync_status()
+    return dq, dk, dv
+
+
+SHAPES = [
+    (1, 1, 128, 128, 64, False),
+    (1, 1, 128, 128, 128, False),
+    (1, 2, 100, 100, 64, True),
+    (1, 2, 100, 100, 128, True),
+    (2, 2, 257, 257, 128, True),
+    (1, 2, 300, 300, 64, False),
+    (1, 1, 200, 333, 128, False),
+    (1, 1, 333, 200, 64, False),
+    (1, 2, 1000, 1000, 128, True),
+    (1, 1, 1, 130, 128, False),
+    (1, 1, 640, 640, 64, True),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_bwd_matches_oracle(shape):
+    require_gpu()
+    B, H, nq, nkv, d, causal = shape
+    x = inputs.make_qkv(B, H, nq, nkv, d, seed=11 + nq + d)
+    scale = d ** -0.5
+    dq, dk, dv = run_fwd_bwd(x, causal, scale)
+    rq, rk, rv, _ = A.backward(x["q"], x["k"], x["v"], x["do"], scale, causal)
+    assert_grad_close(dq, rq, "dQ")
+    assert_grad_close(dk, rk, "dK")
+    assert_grad_close(dv, rv, "dV")
+
+
+def test_bwd_tiny_workload():
+    require_gpu()
+    w = inputs.TINY
+    x = inputs.make_workload(w)
+    dq, dk, dv = run_fwd_bwd(x, w.causal, w.scale)
+    rq, rk, rv, _ = A.backward(x["q"], x["k"], x["v"], x["do"], w.scale, w.causal)
+    assert_grad_close(dq, rq, "dQ")
+    assert_grad_close(dk, rk, "dK")
+    assert_grad_close(dv, rv, "dV")
+
+
+def test_bwd_gpt2m_workload_all_heads():
+    require_gpu()
+    w = inputs.GPT2M
+    x = inputs.make_workload(w)
+    dq, dk, dv = run_fwd_bwd(x, w.causal, w.scale)
+    rq, rk, rv, _ = A.backward(x["q"], x["k"], x["v"], x["do"], w.scale, w.causal)
+    assert_grad_close(dq, rq, "dQ")
+    assert_grad_close(dk, rk, "dK")
+    assert_grad_close(dv, rv, "dV")
+
+
+def _sampled_heads(w, heads, n_rows=48, seed=1):
+    x = inputs.make_workload(w)
+    dq, dk, dv = run_fwd_bwd(x, w.causal, w.scale)
+    dq, dk, dv = dq.cpu(), dk.cpu(), dv.cpu()
+    g = np.random.default_rng(seed)
+    n = w.N_q
+    fixed = np.array([0, 1, 127, 128, n // 2, n - 1])
+    for bh in heads:
+        b, h = divmod(bh, w.H)
+        qr = np.unique(np.concatenate([fixed, g.integers(0, n, n_rows)]))
+        kr = np.unique(np.concatenate([fixed, g.integers(0, w.N_kv, n_rows)]))
+        rq, rk, rv = A.backward_sampled(x["q"][b, h], x["k"][b, h], x["v"][b, h], x["do"][b, h],
+                                        w.scale, w.causal, qr, kr)
+        # relative to the largest magnitude of the whole tensor of this head
+        full_q = np.abs(dq[b, h].double().numpy()).max()
+        full_k = np.abs(dk[b, h].double().numpy()).max()
+        full_v = np.abs(dv[b, h].double().numpy()).max()
+        for got, ref, name, s in ((dq[b, h, qr], rq, "dQ", full_q), (dk[b, h, kr], rk, "dK", full_k),
+                                  (dv[b, h, kr], rv, "dV", full_v)):
+            got = got.double().numpy()
+            assert np.isfinite(got).all()
+            err = np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-30)
+            assert err <= 2e-2, f"{name} head {bh}: rel err {err:.3e}"
+
+
+@pytest.mark.parametrize("w", [inputs.HEADLINE, inputs.HEADLINE_CAUSAL], ids=lambda w: w.name)
+def test_bwd_headline_workload_sampled(w):
+    require_gpu()
+    _sampled_heads(w, heads=[0, 77, w.B * w.H - 1])
+
+
+def test_bwd_long_workload_with_outliers_sampled():
+    require_gpu()
+    _sampled_heads(inputs.LONG, heads=[0, 15], n_rows=24)
+
+
+def test_bwd_dk_dv_deterministic():
+    require_gpu()
+    x = inputs.make_qkv(1, 2, 512, 512, 128, seed=5)
+    a = run_fwd_bwd(x, True, 0.1)
+    b = run_fwd_bwd(x, True, 0.1)
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])

@@ -310,6 +310,17 @@ def test_backward_vs_torch_autograd_fp64(causal):
     np.testing.assert_allclose(dv, tv.grad.numpy(), atol=1e-12)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_sampled_equals_full_head(causal):
+    q, k, v, do = rng_inputs(18, 1, 1, 90, 90, 8)
+    dq, dk, dv, _ = A.backward_head(q[0, 0], k[0, 0], v[0, 0], do[0, 0], 0.3, causal)
+    qr, kr = np.array([0, 7, 50, 89]), np.array([0, 1, 44, 89])
+    sq, sk, sv = A.backward_sampled(q[0, 0], k[0, 0], v[0, 0], do[0, 0], 0.3, causal, qr, kr, block=32)
+    np.testing.assert_allclose(sq, dq[qr], atol=1e-13)
+    np.testing.assert_allclose(sk, dk[kr], atol=1e-13)
+    np.testing.assert_allclose(sv, dv[kr], atol=1e-13)
+
+
 def test_D_identity_rowsum_do_o():
     """Lesson4 §3 'Backward pass', step 3: D_i = sum_j P_ij dP_ij = dO_i . O_i."""
     q, k, v, do = rng_inputs(15, 1, 3, 33, 33, 8)
