@@ -12,7 +12,7 @@
 //   F2  bwd_pre:   D = rowsum(dO o O) in fp32; zero the fp32 dQ accumulator.
 //   F3  bwd_main:  one CTA per (128-key tile, head); 320 threads:
 //         warp 0     TMA producer: K_j, V_j once; Q_i, dO_i (+ lse_i, D_i) per query tile
-//                    through a 2-deep ring.
+//                    through a 3-deep ring.
 //         warp 1     TMEM owner and MMA issuer: S^T = K Q^T, dP^T = V dO^T (keys on TMEM
 //                    lanes), dV += P^T dO, dK += dS^T Q, and the dQ tile product.
 //         warps 2-5  thread = key row: P^T = 2^{S^T scale log2e - lse log2e} (masked), dS^T;
@@ -20,7 +20,8 @@
 //                    dK (times scale) and dV through TMA stores.
 //         warps 6-9  drain the dQ tile from TMEM into the fp32 accumulator with vector
 //                    reductions (red.global.add), overlapping the next tile's MMAs.
-//       TMEM (512 columns): dV, dK (d each), S^T, dP^T (BM each), dQ tile (64).
+//       TMEM (512 columns): dV, dK (d each), S^T, dP^T (BM each), two dQ tiles (64 each), so
+//       the dQ drain of step i overlaps the dQ product of step i+1.
 //       d = 128 uses 64-query steps and forms dQ^T = K^T dS^T (d on TMEM lanes);
 //       d = 64 uses 128-query steps and forms dQ = dS K (queries on TMEM lanes).
 //   F4  bwd_dq_convert: dq = bf16(scale * dQ_acc).
@@ -42,7 +43,7 @@ struct BwdCfg {
   static constexpr int Q_TILE = BM * D * 2;
   static constexpr int Q_CHUNK = BM * 128;          // [BM rows x 64 cols] swizzled
   static constexpr int PT_TILE = BN * BM * 2;       // P^T or dS^T, [QCH][128][64]
-  static constexpr int NST = 2;
+  static constexpr int NST = 3;
   static constexpr int STAGE = 2 * Q_TILE + 1024;   // Q, dO, then lse2[BM], delta[BM]
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = KV_TILE;
@@ -51,8 +52,8 @@ struct BwdCfg {
   static constexpr int OFF_DS = OFF_PT + PT_TILE;
   static constexpr int OFF_BAR = OFF_DS + PT_TILE;
   // kv_full, stage_full[NST], stage_empty[NST], st_full, st_free, pds_ready, pds_free,
-  // dq_full, dq_free, mma_done
-  static constexpr int NBAR = 1 + 2 * NST + 7;
+  // dq_full[2], dq_free[2], mma_done
+  static constexpr int NBAR = 1 + 2 * NST + 9;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -60,9 +61,9 @@ struct BwdCfg {
   static constexpr uint32_t T_DK = D;
   static constexpr uint32_t T_S = 2 * D;
   static constexpr uint32_t T_DP = 2 * D + BM;
-  static constexpr uint32_t T_DQ = 2 * D + 2 * BM;
+  static constexpr uint32_t T_DQ = 2 * D + 2 * BM;  // two dQ tile buffers of 64 columns
   static constexpr int THREADS = 320;
-  static_assert(T_DQ + 64 <= TMEM_COLS, "TMEM budget");
+  static_assert(T_DQ + 128 <= TMEM_COLS, "TMEM budget");
 };
 
 struct BwdParams {
@@ -88,8 +89,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 bwd_main_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = align_smem_1k(smem_raw);
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
   uint8_t* sPT = smem + C::OFF_PT;
@@ -102,9 +102,9 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
   uint64_t* st_free = st_full + 1;
   uint64_t* pds_ready = st_free + 1;
   uint64_t* pds_free = pds_ready + 1;
-  uint64_t* dq_full = pds_free + 1;
-  uint64_t* dq_free = dq_full + 1;
-  uint64_t* mma_done = dq_free + 1;
+  uint64_t* dq_full = pds_free + 1;      // [2], one per dQ TMEM buffer
+  uint64_t* dq_free = dq_full + 2;       // [2]
+  uint64_t* mma_done = dq_free + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -130,8 +130,10 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
     mbar_init(st_free, 128);
     mbar_init(pds_ready, 128);
     mbar_init(pds_free, 1);
-    mbar_init(dq_full, 1);
-    mbar_init(dq_free, 128);
+    for (int b2 = 0; b2 < 2; ++b2) {
+      mbar_init(&dq_full[b2], 1);
+      mbar_init(&dq_free[b2], 128);
+    }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
@@ -240,8 +242,9 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
           umma_ss(tbase + C::T_DK, smem_desc_sw128(ds_addr + a_off, 0, 1024),
                   smem_desc_sw128(st + ks * 2048, C::Q_CHUNK, 1024), id_acc, acc);
         }
-        if (i > 0) {
-          if (!(ok = mbar_wait(dq_free, (i - 1) & 1, abort_flag, 216))) break;
+        const int qb = i & 1;                    // dQ TMEM buffer of this step
+        if (i >= 2) {
+          if (!(ok = mbar_wait(&dq_free[qb], ((i >> 1) - 1) & 1, abort_flag, 216))) break;
           tc_fence_after();
         }
 #pragma unroll
@@ -250,10 +253,10 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
           // d = 64:  dQ   = dS K     (A = dS^T as MN-major, B = K as MN-major)
           const uint64_t kd = smem_desc_sw128(k_addr + ks * 2048, C::KV_CHUNK, 1024);
           const uint64_t dd = smem_desc_sw128(ds_addr + ks * 2048, C::KV_CHUNK, 1024);
-          if constexpr (D == 128) umma_ss(tbase + C::T_DQ, kd, dd, id_dq, ks > 0);
-          else umma_ss(tbase + C::T_DQ, dd, kd, id_dq, ks > 0);
+          if constexpr (D == 128) umma_ss(tbase + C::T_DQ + qb * 64, kd, dd, id_dq, ks > 0);
+          else umma_ss(tbase + C::T_DQ + qb * 64, dd, kd, id_dq, ks > 0);
         }
-        umma_commit(dq_full);
+        umma_commit(&dq_full[qb]);
         umma_commit(pds_free);
         umma_commit(&stage_empty[s]);
       }
@@ -284,15 +287,24 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
         uint32_t rs[32], rd[32];
         tmem_ld32(tbase + t_lane + C::T_S + c * 32, rs);
         tmem_ld32(tbase + t_lane + C::T_DP + c * 32, rd);
+        // per-column lse (log2 units) and D: the same for every thread, read as broadcasts
+        float lv[32], dl[32];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 a = *reinterpret_cast<const float4*>(s_lse + c * 32 + e);
+          const float4 b4 = *reinterpret_cast<const float4*>(s_del + c * 32 + e);
+          lv[e] = a.x; lv[e + 1] = a.y; lv[e + 2] = a.z; lv[e + 3] = a.w;
+          dl[e] = b4.x; dl[e + 1] = b4.y; dl[e + 2] = b4.z; dl[e + 3] = b4.w;
+        }
         tmem_wait_ld();
         float pv[32], dsv[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const int col = c * 32 + e;
-          float pe = fast_exp2(fmaf(__uint_as_float(rs[e]), c2, -s_lse[col]));
+          float pe = fast_exp2(fmaf(__uint_as_float(rs[e]), c2, -lv[e]));
           if (row_dead || (diag && k_idx > q0 + col)) pe = 0.f;
           pv[e] = pe;
-          dsv[e] = pe * (__uint_as_float(rd[e]) - s_del[col]);
+          dsv[e] = pe * (__uint_as_float(rd[e]) - dl[e]);
         }
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
@@ -365,12 +377,13 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
     const uint32_t t_lane = static_cast<uint32_t>(sub * 32) << 16;
     for (int i = 0; i < n; ++i) {
       const int q0 = (i_start + i) * C::BM;
-      if (!mbar_wait_warp(dq_full, i & 1, abort_flag, 231)) break;
+      const int qb = i & 1;
+      if (!mbar_wait_warp(&dq_full[qb], (i >> 1) & 1, abort_flag, 231)) break;
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t v[32];
-        tmem_ld32(tbase + t_lane + C::T_DQ + c * 32, v);
+        tmem_ld32(tbase + t_lane + C::T_DQ + qb * 64 + c * 32, v);
         tmem_wait_ld();
         if constexpr (D == 128) {
           // lane = d, columns = queries q0 + c*32 + e
@@ -390,7 +403,7 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
         }
       }
       tc_fence_before();
-      mbar_arrive(dq_free);
+      mbar_arrive(&dq_free[qb]);
     }
   }
 

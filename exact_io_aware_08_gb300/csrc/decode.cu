@@ -56,8 +56,7 @@ __global__ void __launch_bounds__(DecCfg<D>::THREADS, 2)
 decode_split_kernel(const __grid_constant__ DecParams p) {
   using C = DecCfg<D>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = align_smem_1k(smem_raw);
   float* merge = reinterpret_cast<float*>(smem + C::OFF_MERGE);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + C::NST;

@@ -20,6 +20,13 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// 1 KB-aligned start of the dynamic shared-memory window, derived by pointer arithmetic on the
+// __shared__ array itself so the compiler keeps the shared address space (LDS/STS, not generic
+// loads and stores).  Kernels reserve 1 KB of slack for it.
+__device__ __forceinline__ uint8_t* align_smem_1k(uint8_t* raw) {
+  return raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
