@@ -1,0 +1,563 @@
+// F2/F3/F4: attention backward on sm_103a.
+//
+// Follows "FlashAttention and online softmax" (ML Systems lesson 4), section 3 "Backward pass:
+// recompute instead of store": only O and lse are kept from the forward pass; every tile of P
+// is rebuilt on chip as P = e^{S - lse} (no max and no sum needed), then
+//   dV_j += P^T dO_i,  dP = dO_i V_j^T,  dS = P o (dP - D_i),  D_i = dO_i . O_i,
+//   dQ_i += scale dS K_j,  dK_j += scale dS^T Q_i.
+// The pages leave the loop order of the backward open; this file takes the plainest reading of
+// the "+=" in steps 2 and 4: K_j and V_j stay on chip for a whole CTA (dK_j, dV_j accumulate in
+// TMEM, written once), query tiles stream, and dQ is accumulated across key tiles in fp32.
+//
+//   F2  bwd_pre:   D = rowsum(dO o O) in fp32; zero the fp32 dQ accumulator.
+//   F3  bwd_main:  one CTA per (128-key tile, head); 448 threads:
+//         warp 0     TMA producer: K_j, V_j once; Q_i, dO_i (+ lse_i, D_i) per query tile
+//                    through a 3-deep ring.
+//         warp 1     TMEM owner and MMA issuer: S^T = K Q^T, dP^T = V dO^T (keys on TMEM
+//                    lanes), dV += P^T dO, dK += dS^T Q, and the dQ tile product.
+//         warps 2-9  two warpgroups, thread = (key row, half of the query columns):
+//                    P^T = 2^{S^T scale log2e - lse log2e} (masked), dS^T = P^T o (dP^T - D),
+//                    both written as bf16 to shared memory as MMA operands.  Epilogue: one
+//                    group writes dV, the other dK (times scale), through TMA stores.
+//         warps 10-13 drain the dQ tile from TMEM into the fp32 accumulator with vector
+//                    reductions (red.global.add), overlapping the next tile's MMAs.
+//       TMEM (512 columns): dV, dK (d each), S^T, dP^T (BM each), two dQ tiles (64 each), so
+//       the dQ drain of step i overlaps the dQ product of step i+1.
+//       d = 128 uses 64-query steps and forms dQ^T = K^T dS^T (d on TMEM lanes);
+//       d = 64 uses 128-query steps and forms dQ = dS K (queries on TMEM lanes).
+//   F4  bwd_dq_convert: dq = bf16(scale * dQ_acc).
+#include <algorithm>
+
+#include "../../exact_io_aware_08_gb300/csrc/fa_kernels.h"
+#include "../../exact_io_aware_08_gb300/csrc/sm103.cuh"
+
+namespace fa {
+__device__ unsigned long long g_trace[4][16][64];
+__device__ __forceinline__ int trace_slot() {
+  const unsigned b = blockIdx.x;
+  return b == 0 ? 0 : b == 1 ? 1 : b == 777 ? 2 : b == 1500 ? 3 : -1;
+}
+#define TR(ev, i) do { int _s = trace_slot(); if (_s >= 0 && (i) < 64 && (i) >= 0) g_trace[_s][ev][i] = clock64(); } while (0)
+
+template <int D>
+struct BwdCfg {
+  static constexpr int BN = 128;                    // keys per CTA
+  static constexpr int BM = (D == 128) ? 64 : 128;  // queries per step
+  static constexpr int KCH = D / 64;
+  static constexpr int QCH = BM / 64;
+  static constexpr int KV_TILE = BN * D * 2;
+  static constexpr int KV_CHUNK = BN * 128;         // [128 rows x 64 cols] swizzled
+  static constexpr int Q_TILE = BM * D * 2;
+  static constexpr int Q_CHUNK = BM * 128;          // [BM rows x 64 cols] swizzled
+  static constexpr int PT_TILE = BN * BM * 2;       // P^T or dS^T, [QCH][128][64]
+  static constexpr int NST = 3;
+  static constexpr int STAGE = 2 * Q_TILE + 1024;   // Q, dO, then lse2[BM], delta[BM]
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = KV_TILE;
+  static constexpr int OFF_ST = 2 * KV_TILE;
+  static constexpr int OFF_PT = OFF_ST + NST * STAGE;
+  static constexpr int OFF_DS = OFF_PT + PT_TILE;
+  static constexpr int OFF_BAR = OFF_DS + PT_TILE;
+  // kv_full, stage_full[NST], stage_empty[NST], st_full, st_free, pds_ready, pds_free,
+  // dq_full[2], dq_free[2], mma_done
+  static constexpr int NBAR = 1 + 2 * NST + 9;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static constexpr uint32_t T_DV = 0;
+  static constexpr uint32_t T_DK = D;
+  static constexpr uint32_t T_S = 2 * D;
+  static constexpr uint32_t T_DP = 2 * D + BM;
+  static constexpr uint32_t T_DQ = 2 * D + 2 * BM;  // two dQ tile buffers of 64 columns
+  static constexpr int THREADS = 448;
+  static constexpr int DS_THREADS = 256;          // two dS warpgroups
+  static constexpr int HALF = BM / 2;             // query columns per dS warpgroup
+  static_assert(T_DQ + 128 <= TMEM_COLS, "TMEM budget");
+};
+
+struct BwdParams {
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+  const float* lse;
+  const float* delta;
+  float* dq_acc;
+  int n_q, n_kv, n_qtiles, n_kvtiles, causal;
+  float scale, scale_log2;
+};
+
+__device__ __forceinline__ void red_add_f32(float* p, float v) {
+  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" :: "l"(p), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float c, float d) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+               :: "l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
+bwd_main_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_smem_1k(smem_raw);
+  uint8_t* sK = smem + C::OFF_K;
+  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sPT = smem + C::OFF_PT;
+  uint8_t* sDS = smem + C::OFF_DS;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* kv_full = bars;
+  uint64_t* stage_full = bars + 1;
+  uint64_t* stage_empty = stage_full + C::NST;
+  uint64_t* st_full = stage_empty + C::NST;
+  uint64_t* st_free = st_full + 1;
+  uint64_t* pds_ready = st_free + 1;
+  uint64_t* pds_free = pds_ready + 1;
+  uint64_t* dq_full = pds_free + 1;      // [2], one per dQ TMEM buffer
+  uint64_t* dq_free = dq_full + 2;       // [2]
+  uint64_t* mma_done = dq_free + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Work item: key tile kt of head bh; causal key tiles with more query tiles run first.
+  const int bh = blockIdx.x / p.n_kvtiles;
+  const int kt = blockIdx.x % p.n_kvtiles;
+  const int k0 = kt * C::BN;
+  const int i_start = p.causal ? (k0 / C::BM) : 0;     // first query tile that sees key k0
+  const int n = max(0, p.n_qtiles - i_start);
+
+  auto stage_ptr = [&](int s) { return smem + C::OFF_ST + s * C::STAGE; };
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(&stage_full[s], 2);      // TMA bytes + the producer warp's lse/D writes
+      mbar_init(&stage_empty[s], 1);
+    }
+    mbar_init(st_full, 1);
+    mbar_init(st_free, C::DS_THREADS);
+    mbar_init(pds_ready, C::DS_THREADS);
+    mbar_init(pds_free, 1);
+    for (int b2 = 0; b2 < 2; ++b2) {
+      mbar_init(&dq_full[b2], 1);
+      mbar_init(&dq_free[b2], 128);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tq);
+    tma_prefetch_desc(&p.tk);
+    tma_prefetch_desc(&p.tv);
+    tma_prefetch_desc(&p.tdo);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (n > 0) {
+      if (lane == 0) {
+        mbar_arrive_expect_tx(kv_full, 2 * C::KV_TILE);
+        for (int c = 0; c < C::KCH; ++c) {
+          tma_load_3d(sK + c * C::KV_CHUNK, &p.tk, kv_full, c * 64, k0, bh);
+          tma_load_3d(sV + c * C::KV_CHUNK, &p.tv, kv_full, c * 64, k0, bh);
+        }
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int i = 0; i < n; ++i) {
+        const int s = i % C::NST;
+        const uint32_t u = i / C::NST;
+        if (u > 0 && !(ok = mbar_wait_warp(&stage_empty[s], (u - 1) & 1, abort_flag, 201))) break;
+        if (lane == 0) TR(0, i);
+        uint8_t* st = stage_ptr(s);
+        const int q0 = (i_start + i) * C::BM;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&stage_full[s], 2 * C::Q_TILE);
+          for (int c = 0; c < C::KCH; ++c) {
+            tma_load_3d(st + c * C::Q_CHUNK, &p.tq, &stage_full[s], c * 64, q0, bh);
+            tma_load_3d(st + C::Q_TILE + c * C::Q_CHUNK, &p.tdo, &stage_full[s], c * 64, q0, bh);
+          }
+        }
+        float* s_lse = reinterpret_cast<float*>(st + 2 * C::Q_TILE);
+        float* s_del = s_lse + C::BM;
+        const size_t rowbase = static_cast<size_t>(bh) * p.n_q;
+        for (int e = lane; e < C::BM; e += 32) {
+          const int q = q0 + e;
+          s_lse[e] = (q < p.n_q) ? p.lse[rowbase + q] * 1.4426950408889634f : INFINITY;
+          s_del[e] = (q < p.n_q) ? p.delta[rowbase + q] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) { mbar_arrive(&stage_full[s]); TR(1, i); }
+        issued = i + 1;
+      }
+      if (!ok && lane == 0) {
+        mbar_wait(kv_full, 0, nullptr, 202);
+        for (int i = max(0, issued - C::NST); i < issued; ++i)
+          mbar_wait(&stage_full[i % C::NST], (i / C::NST) & 1, nullptr, 203);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n > 0) {
+      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+      const uint32_t pt_addr = smem_u32(sPT), ds_addr = smem_u32(sDS);
+      const uint32_t id_s = idesc_bf16_f32(128, C::BM, 0, 0);     // K/V K-major, Q/dO K-major
+      const uint32_t id_acc = idesc_bf16_f32(128, D, 0, 1);       // P^T/dS^T K-major, dO/Q MN-major
+      const uint32_t id_dq = idesc_bf16_f32(128, 64, 1, 1);       // both MN-major
+      auto issue_s_dp = [&](int i) {
+        const uint32_t st = smem_u32(stage_ptr(i % C::NST));
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t kv_off = (ks >> 2) * C::KV_CHUNK + (ks & 3) * 32;
+          const uint32_t q_off = (ks >> 2) * C::Q_CHUNK + (ks & 3) * 32;
+          umma_ss(tbase + C::T_S, smem_desc_sw128(k_addr + kv_off, 0, 1024),
+                  smem_desc_sw128(st + q_off, 0, 1024), id_s, ks > 0);
+          umma_ss(tbase + C::T_DP, smem_desc_sw128(v_addr + kv_off, 0, 1024),
+                  smem_desc_sw128(st + C::Q_TILE + q_off, 0, 1024), id_s, ks > 0);
+        }
+        umma_commit(st_full);
+      };
+      bool ok = mbar_wait(kv_full, 0, abort_flag, 211) &&
+                mbar_wait(&stage_full[0], 0, abort_flag, 212);
+      if (ok) {
+        tc_fence_after();
+        issue_s_dp(0);
+        TR(2, 0);
+      }
+      for (int i = 0; ok && i < n; ++i) {
+        const int s = i % C::NST;
+        if (i + 1 < n) {
+          if (!(ok = mbar_wait(st_free, i & 1, abort_flag, 213))) break;
+          if (!(ok = mbar_wait(&stage_full[(i + 1) % C::NST], ((i + 1) / C::NST) & 1, abort_flag, 214)))
+            break;
+          tc_fence_after();
+          issue_s_dp(i + 1);
+          TR(2, i + 1);
+        }
+        if (!(ok = mbar_wait(pds_ready, i & 1, abort_flag, 215))) break;
+        TR(3, i);
+        tc_fence_after();
+        const uint32_t st = smem_u32(stage_ptr(s));
+#pragma unroll
+        for (int ks = 0; ks < C::BM / 16; ++ks) {
+          const uint32_t a_off = (ks >> 2) * C::KV_CHUNK + (ks & 3) * 32;
+          const uint32_t acc = (i > 0 || ks > 0) ? 1u : 0u;
+          // dV += P^T dO
+          umma_ss(tbase + C::T_DV, smem_desc_sw128(pt_addr + a_off, 0, 1024),
+                  smem_desc_sw128(st + C::Q_TILE + ks * 2048, C::Q_CHUNK, 1024), id_acc, acc);
+          // dK += dS^T Q
+          umma_ss(tbase + C::T_DK, smem_desc_sw128(ds_addr + a_off, 0, 1024),
+                  smem_desc_sw128(st + ks * 2048, C::Q_CHUNK, 1024), id_acc, acc);
+        }
+        const int qb = i & 1;                    // dQ TMEM buffer of this step
+        if (i >= 2) {
+          if (!(ok = mbar_wait(&dq_free[qb], ((i >> 1) - 1) & 1, abort_flag, 216))) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int ks = 0; ks < C::BN / 16; ++ks) {
+          // d = 128: dQ^T = K^T dS^T (A = K as MN-major, B = dS^T as MN-major)
+          // d = 64:  dQ   = dS K     (A = dS^T as MN-major, B = K as MN-major)
+          const uint64_t kd = smem_desc_sw128(k_addr + ks * 2048, C::KV_CHUNK, 1024);
+          const uint64_t dd = smem_desc_sw128(ds_addr + ks * 2048, C::KV_CHUNK, 1024);
+          if constexpr (D == 128) umma_ss(tbase + C::T_DQ + qb * 64, kd, dd, id_dq, ks > 0);
+          else umma_ss(tbase + C::T_DQ + qb * 64, dd, kd, id_dq, ks > 0);
+        }
+        TR(4, i);
+        umma_commit(&dq_full[qb]);
+        umma_commit(pds_free);
+        umma_commit(&stage_empty[s]);
+      }
+      umma_commit(mma_done);
+      mbar_wait(mma_done, 0, nullptr, 217);
+    }
+  } else if (warp < 10) {
+    // ------------------------------------------------------------------ dS warpgroups
+    const int sub = warp & 3;
+    const int grp = (warp - 2) >> 2;               // which half of the query columns
+    const int cb = grp * C::HALF;                  // first column of this group
+    const int r = sub * 32 + lane;                 // key row within the tile
+    const uint32_t t_lane = static_cast<uint32_t>(sub * 32) << 16;
+    const int k_idx = k0 + r;
+    const bool row_dead = k_idx >= p.n_kv;
+    const float c2 = p.scale_log2;
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      const int q0 = (i_start + i) * C::BM;
+      if (!(ok = mbar_wait_warp(st_full, i & 1, abort_flag, 221))) break;
+      if (threadIdx.x == 64) TR(5, i);
+      // lse/D of this stage were written by the producer warp: acquire them directly
+      if (!(ok = mbar_wait_warp(&stage_full[i % C::NST], (i / C::NST) & 1, abort_flag, 224))) break;
+      tc_fence_after();
+      const float* s_lse = reinterpret_cast<const float*>(stage_ptr(i % C::NST) + 2 * C::Q_TILE);
+      const float* s_del = s_lse + C::BM;
+      const bool diag = p.causal && (q0 < k0 + C::BN - 1);
+      uint32_t pk_p[C::HALF / 2], pk_ds[C::HALF / 2];
+#pragma unroll
+      for (int c = 0; c < C::HALF / 32; ++c) {
+        uint32_t rs[32], rd[32];
+        tmem_ld32(tbase + t_lane + C::T_S + cb + c * 32, rs);
+        tmem_ld32(tbase + t_lane + C::T_DP + cb + c * 32, rd);
+        // per-column lse (log2 units) and D: the same for every thread, read as broadcasts
+        float lv[32], dl[32];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 a = *reinterpret_cast<const float4*>(s_lse + cb + c * 32 + e);
+          const float4 b4 = *reinterpret_cast<const float4*>(s_del + cb + c * 32 + e);
+          lv[e] = a.x; lv[e + 1] = a.y; lv[e + 2] = a.z; lv[e + 3] = a.w;
+          dl[e] = b4.x; dl[e + 1] = b4.y; dl[e + 2] = b4.z; dl[e + 3] = b4.w;
+        }
+        tmem_wait_ld();
+        float pv[32], dsv[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int col = cb + c * 32 + e;
+          float pe = fast_exp2(fmaf(__uint_as_float(rs[e]), c2, -lv[e]));
+          if (row_dead || (diag && k_idx > q0 + col)) pe = 0.f;
+          pv[e] = pe;
+          dsv[e] = pe * (__uint_as_float(rd[e]) - dl[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          pk_p[c * 16 + e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
+          pk_ds[c * 16 + e] = pack_bf16x2(dsv[2 * e], dsv[2 * e + 1]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(st_free);
+      if (threadIdx.x == 64) TR(6, i);
+      if (i > 0 && !(ok = mbar_wait_warp(pds_free, (i - 1) & 1, abort_flag, 222))) break;
+      if (threadIdx.x == 64) TR(7, i);
+#pragma unroll
+      for (int u = 0; u < C::HALF / 8; ++u) {
+        const int c8 = cb / 8 + u;                   // 16-byte unit along the query axis
+        const uint32_t off = (c8 >> 3) * C::KV_CHUNK + sw128_offset(r, (c8 & 7) * 8);
+        *reinterpret_cast<uint4*>(sPT + off) =
+            make_uint4(pk_p[4 * u], pk_p[4 * u + 1], pk_p[4 * u + 2], pk_p[4 * u + 3]);
+        *reinterpret_cast<uint4*>(sDS + off) =
+            make_uint4(pk_ds[4 * u], pk_ds[4 * u + 1], pk_ds[4 * u + 2], pk_ds[4 * u + 3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(pds_ready);
+      if (threadIdx.x == 64) TR(8, i);
+    }
+    // ---------------------------------------------------------------- epilogue: dK, dV
+    if (ok && n > 0) {
+      ok = mbar_wait_warp(mma_done, 0, abort_flag, 223);
+      tc_fence_after();
+    }
+    if (ok) {
+      {
+        const int which = grp;                        // group 0 writes dV, group 1 dK
+        uint8_t* dst = which ? sK : sV;               // operands are dead once mma_done fired
+        const uint32_t tcol = which ? C::T_DK : C::T_DV;
+        const float mul = which ? p.scale : 1.f;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t rr[32];
+          if (n > 0) {
+            tmem_ld32(tbase + t_lane + tcol + c * 32, rr);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) rr[e] = 0u;
+          }
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 v4;
+            v4.x = pack_bf16x2(__uint_as_float(rr[e + 0]) * mul, __uint_as_float(rr[e + 1]) * mul);
+            v4.y = pack_bf16x2(__uint_as_float(rr[e + 2]) * mul, __uint_as_float(rr[e + 3]) * mul);
+            v4.z = pack_bf16x2(__uint_as_float(rr[e + 4]) * mul, __uint_as_float(rr[e + 5]) * mul);
+            v4.w = pack_bf16x2(__uint_as_float(rr[e + 6]) * mul, __uint_as_float(rr[e + 7]) * mul);
+            const int col = c * 32 + e;
+            *reinterpret_cast<uint4*>(dst + (col >> 6) * C::KV_CHUNK + sw128_offset(r, col & 63)) = v4;
+          }
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    named_bar_sync(1, C::DS_THREADS);
+    if (ok && threadIdx.x == 64) {
+      for (int c = 0; c < C::KCH; ++c) {
+        tma_store_3d(&p.tdk, sK + c * C::KV_CHUNK, c * 64, k0, bh);
+        tma_store_3d(&p.tdv, sV + c * C::KV_CHUNK, c * 64, k0, bh);
+      }
+      bulk_commit_group();
+      bulk_wait_group_read0();
+    }
+  } else {
+    // ------------------------------------------------------------------ dQ warpgroup
+    const int sub = warp & 3;
+    const int rr_ = sub * 32 + lane;               // TMEM lane: d (d=128) or query (d=64)
+    const uint32_t t_lane = static_cast<uint32_t>(sub * 32) << 16;
+    for (int i = 0; i < n; ++i) {
+      const int q0 = (i_start + i) * C::BM;
+      const int qb = i & 1;
+      if (!mbar_wait_warp(&dq_full[qb], (i >> 1) & 1, abort_flag, 231)) break;
+      if (threadIdx.x == 192) TR(9, i);
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tbase + t_lane + C::T_DQ + qb * 64 + c * 32, v);
+        tmem_wait_ld();
+        if constexpr (D == 128) {
+          // lane = d, columns = queries q0 + c*32 + e
+          float* base = p.dq_acc + (static_cast<size_t>(bh) * p.n_q + q0 + c * 32) * D + rr_;
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (q0 + c * 32 + e < p.n_q) red_add_f32(base + static_cast<size_t>(e) * D, __uint_as_float(v[e]));
+        } else {
+          // lane = query q0 + rr_, columns = d
+          if (q0 + rr_ < p.n_q) {
+            float* base = p.dq_acc + (static_cast<size_t>(bh) * p.n_q + q0 + rr_) * D + c * 32;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              red_add_v4_f32(base + e, __uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                             __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&dq_free[qb]);
+      if (threadIdx.x == 192) TR(10, i);
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+}
+
+// F2: D = rowsum(dO o O) (fp32) and zero the dQ accumulator.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict__ o,
+                                                      const uint16_t* __restrict__ dO,
+                                                      float* __restrict__ delta,
+                                                      float4* __restrict__ dq_acc4,
+                                                      long long rows, long long acc4) {
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long nthr = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long x = tid; x < acc4; x += nthr) dq_acc4[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int TPR = D / 8;                        // threads per row, 8 bf16 each
+  constexpr int RPW = 32 / TPR;                     // rows per warp and pass
+  const int lane = threadIdx.x & 31;
+  const int part = lane % TPR;
+  const long long ngrp = nthr / TPR;
+  // warp-uniform trip count so the shuffles below always see all 32 lanes
+  for (long long r0 = (tid >> 5) * RPW; r0 < rows; r0 += ngrp) {
+    const long long row = r0 + lane / TPR;
+    const bool valid = row < rows;
+    float s = 0.f;
+    if (valid) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + row * D) + part);
+      const uint4 b = __ldg(reinterpret_cast<const uint4*>(dO + row * D) + part);
+      const uint32_t aa[4] = {a.x, a.y, a.z, a.w}, bb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        s = fmaf(__uint_as_float(aa[e] << 16), __uint_as_float(bb[e] << 16), s);
+        s = fmaf(__uint_as_float(aa[e] & 0xffff0000u), __uint_as_float(bb[e] & 0xffff0000u), s);
+      }
+    }
+#pragma unroll
+    for (int off = TPR / 2; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (valid && part == 0) delta[row] = s;
+  }
+}
+
+// F4: dq = bf16(scale * dQ_acc)
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4* __restrict__ acc,
+                                                             uint2* __restrict__ dq, float scale,
+                                                             long long n4) {
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long nthr = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long x = tid; x < n4; x += nthr) {
+    const float4 v = acc[x];
+    dq[x] = make_uint2(pack_bf16x2(v.x * scale, v.y * scale), pack_bf16x2(v.z * scale, v.w * scale));
+  }
+}
+
+template <int D>
+static cudaError_t launch_bwd_prep_d(const BwdArgs& a, cudaStream_t stream) {
+  const uint64_t bh = static_cast<uint64_t>(a.B) * a.H;
+  const long long rows = static_cast<long long>(bh) * a.n_q;
+  if (rows == 0) return cudaSuccess;
+  const long long acc4 = rows * D / 4;
+  const int blocks = static_cast<int>(std::min<long long>(152LL * 8, (rows * (D / 8) + 255) / 256));
+  bwd_pre_kernel<D><<<std::max(blocks, 1), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dO), a.delta,
+      reinterpret_cast<float4*>(a.dq_acc), rows, acc4);
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_bwd_main_d(const BwdArgs& a, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  if (a.n_kv == 0) return cudaSuccess;
+  const uint64_t bh = static_cast<uint64_t>(a.B) * a.H;
+  BwdParams p;
+  const uint64_t nq = a.n_q > 0 ? a.n_q : 1;
+  const void* qb = a.n_q > 0 ? a.q : a.k;
+  const void* dob = a.n_q > 0 ? a.dO : a.k;
+  if (!make_map_bf16_3d(&p.tq, qb, D, nq, bh, 64, C::BM) ||
+      !make_map_bf16_3d(&p.tdo, dob, D, nq, bh, 64, C::BM) ||
+      !make_map_bf16_3d(&p.tk, a.k, D, a.n_kv, bh, 64, C::BN) ||
+      !make_map_bf16_3d(&p.tv, a.v, D, a.n_kv, bh, 64, C::BN) ||
+      !make_map_bf16_3d(&p.tdk, a.dk, D, a.n_kv, bh, 64, C::BN) ||
+      !make_map_bf16_3d(&p.tdv, a.dv, D, a.n_kv, bh, 64, C::BN))
+    return cudaErrorInvalidValue;
+  p.lse = a.lse;
+  p.delta = a.delta;
+  p.dq_acc = a.dq_acc;
+  p.n_q = a.n_q;
+  p.n_kv = a.n_kv;
+  p.n_qtiles = (a.n_q + C::BM - 1) / C::BM;
+  p.n_kvtiles = (a.n_kv + C::BN - 1) / C::BN;
+  p.causal = a.causal;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  static int attr_done[64] = {0};   // one per instantiation of this launcher
+  cudaError_t e = ensure_smem_attr(bwd_main_kernel<D>, C::SMEM_BYTES, attr_done);
+  if (e != cudaSuccess) return e;
+  const uint64_t grid = static_cast<uint64_t>(p.n_kvtiles) * bh;
+  bwd_main_kernel<D><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_bwd_finish_d(const BwdArgs& a, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(a.B) * a.H * a.n_q;
+  if (rows == 0) return cudaSuccess;
+  const long long n4 = rows * D / 4;
+  const int blocks = static_cast<int>(std::min<long long>(152LL * 8, (n4 + 255) / 256));
+  bwd_dq_convert_kernel<<<std::max(blocks, 1), 256, 0, stream>>>(
+      reinterpret_cast<const float4*>(a.dq_acc), static_cast<uint2*>(a.dq), a.scale, n4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t s) {
+  return a.d == 64 ? launch_bwd_prep_d<64>(a, s) : launch_bwd_prep_d<128>(a, s);
+}
+cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t s) {
+  return a.d == 64 ? launch_bwd_main_d<64>(a, s) : launch_bwd_main_d<128>(a, s);
+}
+cudaError_t launch_bwd_finish(const BwdArgs& a, cudaStream_t s) {
+  return a.d == 64 ? launch_bwd_finish_d<64>(a, s) : launch_bwd_finish_d<128>(a, s);
+}
+
+}  // namespace fa
+
+FA_DEFINE_STATUS_FETCH(status_fetch_bwd)
+extern "C" int fa_trace_read(void* host) {
+  return (int)cudaMemcpyFromSymbol(host, fa::g_trace, sizeof(fa::g_trace));
+}

@@ -10,15 +10,16 @@
 // TMEM, written once), query tiles stream, and dQ is accumulated across key tiles in fp32.
 //
 //   F2  bwd_pre:   D = rowsum(dO o O) in fp32; zero the fp32 dQ accumulator.
-//   F3  bwd_main:  one CTA per (128-key tile, head); 320 threads:
+//   F3  bwd_main:  one CTA per (128-key tile, head); 448 threads:
 //         warp 0     TMA producer: K_j, V_j once; Q_i, dO_i (+ lse_i, D_i) per query tile
 //                    through a 3-deep ring.
 //         warp 1     TMEM owner and MMA issuer: S^T = K Q^T, dP^T = V dO^T (keys on TMEM
 //                    lanes), dV += P^T dO, dK += dS^T Q, and the dQ tile product.
-//         warps 2-5  thread = key row: P^T = 2^{S^T scale log2e - lse log2e} (masked), dS^T;
-//                    both written as bf16 to shared memory as MMA operands.  Epilogue writes
-//                    dK (times scale) and dV through TMA stores.
-//         warps 6-9  drain the dQ tile from TMEM into the fp32 accumulator with vector
+//         warps 2-9  two warpgroups, thread = (key row, half of the query columns):
+//                    P^T = 2^{S^T scale log2e - lse log2e} (masked), dS^T = P^T o (dP^T - D),
+//                    both written as bf16 to shared memory as MMA operands.  Epilogue: one
+//                    group writes dV, the other dK (times scale), through TMA stores.
+//         warps 10-13 drain the dQ tile from TMEM into the fp32 accumulator with vector
 //                    reductions (red.global.add), overlapping the next tile's MMAs.
 //       TMEM (512 columns): dV, dK (d each), S^T, dP^T (BM each), two dQ tiles (64 each), so
 //       the dQ drain of step i overlaps the dQ product of step i+1.
@@ -62,7 +63,9 @@ struct BwdCfg {
   static constexpr uint32_t T_S = 2 * D;
   static constexpr uint32_t T_DP = 2 * D + BM;
   static constexpr uint32_t T_DQ = 2 * D + 2 * BM;  // two dQ tile buffers of 64 columns
-  static constexpr int THREADS = 320;
+  static constexpr int THREADS = 448;
+  static constexpr int DS_THREADS = 256;          // two dS warpgroups
+  static constexpr int HALF = BM / 2;             // query columns per dS warpgroup
   static_assert(T_DQ + 128 <= TMEM_COLS, "TMEM budget");
 };
 
@@ -127,8 +130,8 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       mbar_init(&stage_empty[s], 1);
     }
     mbar_init(st_full, 1);
-    mbar_init(st_free, 128);
-    mbar_init(pds_ready, 128);
+    mbar_init(st_free, C::DS_THREADS);
+    mbar_init(pds_ready, C::DS_THREADS);
     mbar_init(pds_free, 1);
     for (int b2 = 0; b2 < 2; ++b2) {
       mbar_init(&dq_full[b2], 1);
@@ -263,9 +266,11 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       umma_commit(mma_done);
       mbar_wait(mma_done, 0, nullptr, 217);
     }
-  } else if (warp < 6) {
-    // ------------------------------------------------------------------ dS warpgroup
+  } else if (warp < 10) {
+    // ------------------------------------------------------------------ dS warpgroups
     const int sub = warp & 3;
+    const int grp = (warp - 2) >> 2;               // which half of the query columns
+    const int cb = grp * C::HALF;                  // first column of this group
     const int r = sub * 32 + lane;                 // key row within the tile
     const uint32_t t_lane = static_cast<uint32_t>(sub * 32) << 16;
     const int k_idx = k0 + r;
@@ -281,18 +286,18 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       const float* s_lse = reinterpret_cast<const float*>(stage_ptr(i % C::NST) + 2 * C::Q_TILE);
       const float* s_del = s_lse + C::BM;
       const bool diag = p.causal && (q0 < k0 + C::BN - 1);
-      uint32_t pk_p[C::BM / 2], pk_ds[C::BM / 2];
+      uint32_t pk_p[C::HALF / 2], pk_ds[C::HALF / 2];
 #pragma unroll
-      for (int c = 0; c < C::BM / 32; ++c) {
+      for (int c = 0; c < C::HALF / 32; ++c) {
         uint32_t rs[32], rd[32];
-        tmem_ld32(tbase + t_lane + C::T_S + c * 32, rs);
-        tmem_ld32(tbase + t_lane + C::T_DP + c * 32, rd);
+        tmem_ld32(tbase + t_lane + C::T_S + cb + c * 32, rs);
+        tmem_ld32(tbase + t_lane + C::T_DP + cb + c * 32, rd);
         // per-column lse (log2 units) and D: the same for every thread, read as broadcasts
         float lv[32], dl[32];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          const float4 a = *reinterpret_cast<const float4*>(s_lse + c * 32 + e);
-          const float4 b4 = *reinterpret_cast<const float4*>(s_del + c * 32 + e);
+          const float4 a = *reinterpret_cast<const float4*>(s_lse + cb + c * 32 + e);
+          const float4 b4 = *reinterpret_cast<const float4*>(s_del + cb + c * 32 + e);
           lv[e] = a.x; lv[e + 1] = a.y; lv[e + 2] = a.z; lv[e + 3] = a.w;
           dl[e] = b4.x; dl[e + 1] = b4.y; dl[e + 2] = b4.z; dl[e + 3] = b4.w;
         }
@@ -300,7 +305,7 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
         float pv[32], dsv[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          const int col = c * 32 + e;
+          const int col = cb + c * 32 + e;
           float pe = fast_exp2(fmaf(__uint_as_float(rs[e]), c2, -lv[e]));
           if (row_dead || (diag && k_idx > q0 + col)) pe = 0.f;
           pv[e] = pe;
@@ -316,12 +321,13 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       mbar_arrive(st_free);
       if (i > 0 && !(ok = mbar_wait_warp(pds_free, (i - 1) & 1, abort_flag, 222))) break;
 #pragma unroll
-      for (int c8 = 0; c8 < C::BM / 8; ++c8) {
+      for (int u = 0; u < C::HALF / 8; ++u) {
+        const int c8 = cb / 8 + u;                   // 16-byte unit along the query axis
         const uint32_t off = (c8 >> 3) * C::KV_CHUNK + sw128_offset(r, (c8 & 7) * 8);
         *reinterpret_cast<uint4*>(sPT + off) =
-            make_uint4(pk_p[4 * c8], pk_p[4 * c8 + 1], pk_p[4 * c8 + 2], pk_p[4 * c8 + 3]);
+            make_uint4(pk_p[4 * u], pk_p[4 * u + 1], pk_p[4 * u + 2], pk_p[4 * u + 3]);
         *reinterpret_cast<uint4*>(sDS + off) =
-            make_uint4(pk_ds[4 * c8], pk_ds[4 * c8 + 1], pk_ds[4 * c8 + 2], pk_ds[4 * c8 + 3]);
+            make_uint4(pk_ds[4 * u], pk_ds[4 * u + 1], pk_ds[4 * u + 2], pk_ds[4 * u + 3]);
       }
       fence_proxy_async_smem();
       mbar_arrive(pds_ready);
@@ -332,8 +338,8 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       tc_fence_after();
     }
     if (ok) {
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
+      {
+        const int which = grp;                        // group 0 writes dV, group 1 dK
         uint8_t* dst = which ? sK : sV;               // operands are dead once mma_done fired
         const uint32_t tcol = which ? C::T_DK : C::T_DV;
         const float mul = which ? p.scale : 1.f;
@@ -361,7 +367,7 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       }
       fence_proxy_async_smem();
     }
-    named_bar_sync(1, 128);
+    named_bar_sync(1, C::DS_THREADS);
     if (ok && threadIdx.x == 64) {
       for (int c = 0; c < C::KCH; ++c) {
         tma_store_3d(&p.tdk, sK + c * C::KV_CHUNK, c * 64, k0, bh);
