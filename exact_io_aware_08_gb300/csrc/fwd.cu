@@ -1,22 +1,35 @@
 // F1: attention forward on sm_103a.
 //
 // Follows "FlashAttention and online softmax" (ML Systems lesson 4), section 3 "The tiled
-// forward pass" and "The online softmax theorem": one CTA owns a tile of 128 query rows, keeps
-// Q on chip, streams 128-key tiles of K and V, and carries the per-row state (m, l, o~) across
-// tiles, dividing once at the end (the FlashAttention-2 form, "Keep o~ unnormalised").
-// Causal tiles above the diagonal are skipped, the diagonal tile is masked ("Causal masks").
+// forward pass" and "The online softmax theorem": a query tile stays on chip, 128-key tiles of
+// K and V stream past it, and each row carries its state (m, l, o~) across tiles, dividing once
+// at the end (the FlashAttention-2 form, "Keep o~ unnormalised").  Causal tiles above the
+// diagonal are skipped and the diagonal tile is masked ("Causal masks").
 //
-// GB300 mapping (one CTA per SM, 192 threads):
-//   warp 0      TMA producer: Q once, then K_j / V_j into NST-deep shared-memory rings.
-//   warp 1      TMEM owner and MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
-//               score buffers, then O += P_j V_j into the TMEM output accumulator.
-//   warps 2-5   softmax + correction: thread t owns query row t; it loads its S row from TMEM,
-//               updates (m, l) in the log2 domain (scale * log2 e folded into one FMA), writes
-//               P_j as bf16 into shared memory for the PV MMA, and rescales its O row in TMEM by
-//               e^{m_old - m_new} when the max moved.  The epilogue divides by l, writes O
-//               through a TMA store and lse = m + ln l.
-// The MMA for S_{j+1} is issued before the PV of tile j, so the tensor core computes the next
-// score tile while the softmax warps work on the current one.
+// GB300 mapping.  One CTA (384 threads, one per SM) owns TWO 128-row query tiles of a head,
+// which share every K/V tile loaded into shared memory:
+//   warp 0      TMA producer: Q_0, Q_1 once, then K_j and V_j through NS-deep rings.
+//   warp 1      TMEM owner and single-thread MMA issuer (tcgen05.mma kind::f16, fp32 in TMEM):
+//                 S_t = Q_t K_j^T          A, B from shared memory (both K-major)
+//                 O_t += P_t V_j           A = P_t from TMEM, B = V_j from shared memory
+//               in the order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so the tensor core works
+//               on one tile while the other tile's softmax runs.
+//   warps 2-3   idle (they complete warpgroup 0, which gives up registers with setmaxnreg).
+//   warps 4-7   softmax of tile 0, warps 8-11 softmax of tile 1: thread = query row.  A thread
+//               loads its S row from TMEM, updates (m, l) in the log2 domain (scale * log2 e
+//               folded into one FMA), writes P as bf16 back over its S row in TMEM (P never
+//               touches shared memory), and rescales its O row in TMEM when needed.  The
+//               epilogue divides by l, stores O through TMA and writes lse = m + ln l.
+// TMEM (512 columns): S_0, S_1 (128 each; P_t overwrites the first 64 columns of S_t),
+// O_0, O_1 (d each).  An S_t product is issued after the PV_t product that reads P_t from the
+// same columns; tcgen05.mma operations of one thread execute in issue order.
+//
+// Rescaling.  The online-softmax theorem holds for ANY reference value that l and o~ share:
+// o~/l is unchanged when both are measured against a stale maximum.  So a row moves its
+// reference m to the new running max only when the max grew by more than 2^8 (exp2 units);
+// otherwise it keeps m, and its weights 2^{s - m} stay <= 256 (exact in fp32, no overflow).
+// This skips most O corrections (a published FlashAttention-4 technique); the first tile
+// always sets m.
 #include "fa_kernels.h"
 #include "sm103.cuh"
 
@@ -24,32 +37,35 @@ namespace fa {
 
 template <int D>
 struct FwdCfg {
-  static constexpr int BM = 128;
-  static constexpr int BN = 128;
-  static constexpr int KCH = D / 64;                 // 64-column (128-byte) chunks per row
-  static constexpr int TILE = 128 * D * 2;           // bytes of one 128-row bf16 tile
-  static constexpr int CHUNK = 128 * 128;            // bytes of one [128 x 64] swizzled chunk
-  static constexpr int NST = (D == 128) ? 2 : 4;     // K/V ring depth (one CTA per SM)
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + TILE;
-  static constexpr int OFF_V = OFF_K + NST * TILE;
-  static constexpr int OFF_P = OFF_V + NST * TILE;
-  static constexpr int OFF_BAR = OFF_P + 2 * CHUNK;
-  // q_full, k_full[NST], k_empty[NST], v_full[NST], v_empty[NST], s_full[2], s_free[2],
-  // p_full, o_done, mma_done
-  static constexpr int NBAR = 1 + 4 * NST + 4 + 3;
+  static constexpr int BM = 128;                      // rows per query tile (2 tiles per CTA)
+  static constexpr int BN = 128;                      // keys per K/V tile
+  static constexpr int KCH = D / 64;                  // 64-column (128-byte) chunks per row
+  static constexpr int TILE = 128 * D * 2;            // bytes of one 128-row bf16 tile
+  static constexpr int CHUNK = 128 * 128;             // bytes of one [128 x 64] swizzled chunk
+  static constexpr int NS = (D == 128) ? 2 : 4;       // K ring and V ring depth
+  static constexpr int OFF_Q = 0;                     // Q_0, Q_1 (later: O staging)
+  static constexpr int OFF_K = 2 * TILE;
+  static constexpr int OFF_V = OFF_K + NS * TILE;
+  static constexpr int OFF_BAR = OFF_V + NS * TILE;
+  // q_full, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[2], p_full[2], o_done[2]
+  static constexpr int NBAR = 1 + 4 * NS + 6;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack for 1 KB alignment
   static constexpr uint32_t TMEM_COLS = 512;
-  static constexpr uint32_t T_S = 0;      // two score buffers: columns [0,128) and [128,256)
-  static constexpr uint32_t T_O = 256;    // output accumulator: columns [256, 256 + D)
-  static constexpr int THREADS = 192;
+  static constexpr uint32_t T_S = 0;                  // S_t at columns [128 t, 128 t + 128)
+  static constexpr uint32_t T_O = 256;                // O_t at columns [256 + d t, ...)
+  static constexpr int THREADS = 384;
+  // setmaxnreg split: launched with 168 per thread (384 x 168 = 64512); warpgroup 0 (producer,
+  // MMA) drops to 80, the two softmax warpgroups rise to 208: 128*80 + 2*128*208 = 63488.
+  static constexpr uint32_t REG_CTRL = 80;
+  static constexpr uint32_t REG_SOFTMAX = 208;
+  static constexpr float RESCALE_THRESHOLD = 8.f;     // log2 units: factor 256
 };
 
 struct FwdParams {
   CUtensorMap tq, tk, tv, to;
   float* lse;
-  int n_q, n_kv, bh, n_qtiles, n_kvtiles, causal;
+  int n_q, n_kv, n_qpairs, n_kvtiles, causal;
   float scale, scale_log2;
 };
 
@@ -62,47 +78,48 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
   uint8_t* sQ = smem + C::OFF_Q;
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
-  uint8_t* sP = smem + C::OFF_P;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;
-  uint64_t* k_empty = k_full + C::NST;
-  uint64_t* v_full = k_empty + C::NST;
-  uint64_t* v_empty = v_full + C::NST;
-  uint64_t* s_full = v_empty + C::NST;
-  uint64_t* s_free = s_full + 2;
-  uint64_t* p_full = s_free + 2;
-  uint64_t* o_done = p_full + 1;
-  uint64_t* mma_done = o_done + 1;
+  uint64_t* k_empty = k_full + C::NS;
+  uint64_t* v_full = k_empty + C::NS;
+  uint64_t* v_empty = v_full + C::NS;
+  uint64_t* s_full = v_empty + C::NS;      // [2]
+  uint64_t* p_full = s_full + 2;           // [2]
+  uint64_t* o_done = p_full + 2;           // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work item: query tile qt of head bh.  Tiles of one head are adjacent so the CTAs that run
-  // together share K/V in L2; causal runs the longer (later) tiles of each head first.
-  const int bh = blockIdx.x / p.n_qtiles;
-  const int r = blockIdx.x % p.n_qtiles;
-  const int qt = p.causal ? (p.n_qtiles - 1 - r) : r;
-  const int q0 = qt * C::BM;
-  const int n_tiles = p.causal ? min(qt + 1, p.n_kvtiles) : p.n_kvtiles;
+  // Work item: query rows [256 c, 256 c + 256) of head bh.  Items of one head are adjacent so
+  // the CTAs that run together share K/V in L2; causal runs each head's longer items first.
+  const int bh = blockIdx.x / p.n_qpairs;
+  const int r = blockIdx.x % p.n_qpairs;
+  const int c = p.causal ? (p.n_qpairs - 1 - r) : r;
+  int q0[2], n_t[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    q0[t] = c * 2 * C::BM + t * C::BM;
+    const int tile_index = 2 * c + t;                 // in units of 128 rows
+    n_t[t] = (q0[t] >= p.n_q) ? 0 : (p.causal ? min(tile_index + 1, p.n_kvtiles) : p.n_kvtiles);
+  }
+  const int n_max = max(n_t[0], n_t[1]);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < C::NST; ++s) {
+    for (int s = 0; s < C::NS; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&s_full[b], 1);
-      mbar_init(&s_free[b], 128);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 128);
+      mbar_init(&o_done[t], 1);
     }
-    mbar_init(p_full, 128);
-    mbar_init(o_done, 1);
-    mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -116,180 +133,203 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
-
+  if (warp < 4) {
+  setmaxnreg_dec<C::REG_CTRL>();   // warpgroup 0: producer, MMA issuer, two idle warps
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0 && n_tiles > 0) {
+    if (lane == 0 && n_max > 0) {
       int issued = 0;
-      mbar_arrive_expect_tx(q_full, C::TILE);
-      for (int c = 0; c < C::KCH; ++c) tma_load_3d(sQ + c * C::CHUNK, &p.tq, q_full, c * 64, q0, bh);
-      for (int j = 0; j < n_tiles; ++j) {
-        const int s = j % C::NST;
-        const uint32_t n = j / C::NST;
-        if (n > 0 && !mbar_wait(&k_empty[s], (n - 1) & 1, abort_flag, 101)) break;
+      const int nq_tiles = (n_t[1] > 0) ? 2 : 1;
+      mbar_arrive_expect_tx(q_full, nq_tiles * C::TILE);
+      for (int t = 0; t < nq_tiles; ++t)
+        for (int k = 0; k < C::KCH; ++k)
+          tma_load_3d(sQ + t * C::TILE + k * C::CHUNK, &p.tq, q_full, k * 64, q0[t], bh);
+      for (int j = 0; j < n_max; ++j) {
+        const int s = j % C::NS;
+        const uint32_t u = j / C::NS;
+        if (u > 0 && !mbar_wait(&k_empty[s], (u - 1) & 1, abort_flag, 101)) break;
         mbar_arrive_expect_tx(&k_full[s], C::TILE);
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_3d(sK + s * C::TILE + c * C::CHUNK, &p.tk, &k_full[s], c * 64, j * C::BN, bh);
-        if (n > 0 && !mbar_wait(&v_empty[s], (n - 1) & 1, abort_flag, 102)) break;
+        for (int k = 0; k < C::KCH; ++k)
+          tma_load_3d(sK + s * C::TILE + k * C::CHUNK, &p.tk, &k_full[s], k * 64, j * C::BN, bh);
+        if (u > 0 && !mbar_wait(&v_empty[s], (u - 1) & 1, abort_flag, 102)) break;
         mbar_arrive_expect_tx(&v_full[s], C::TILE);
-        for (int c = 0; c < C::KCH; ++c)
-          tma_load_3d(sV + s * C::TILE + c * C::CHUNK, &p.tv, &v_full[s], c * 64, j * C::BN, bh);
+        for (int k = 0; k < C::KCH; ++k)
+          tma_load_3d(sV + s * C::TILE + k * C::CHUNK, &p.tv, &v_full[s], k * 64, j * C::BN, bh);
         issued = j + 1;
       }
       if (*abort_flag) {
         // Drain: let every copy this thread started land before the CTA exits.
         mbar_wait(q_full, 0, nullptr, 103);
-        for (int j = max(0, issued - C::NST); j < issued; ++j) {
-          mbar_wait(&k_full[j % C::NST], (j / C::NST) & 1, nullptr, 104);
-          mbar_wait(&v_full[j % C::NST], (j / C::NST) & 1, nullptr, 105);
+        for (int j = max(0, issued - C::NS); j < issued; ++j) {
+          mbar_wait(&k_full[j % C::NS], (j / C::NS) & 1, nullptr, 104);
+          mbar_wait(&v_full[j % C::NS], (j / C::NS) & 1, nullptr, 105);
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_tiles > 0) {
+    if (lane == 0 && n_max > 0) {
       const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
-      const uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);    // P K-major, V MN-major
-      const uint32_t q_addr = smem_u32(sQ);
-      const uint32_t p_addr = smem_u32(sP);
-      bool ok = mbar_wait(q_full, 0, abort_flag, 111);
-      auto issue_s = [&](int j) {
-        const int s = j % C::NST;
-        const uint32_t k_addr = smem_u32(sK + s * C::TILE);
-        const uint32_t d_tmem = tbase + C::T_S + (j & 1) * 128;
+      const uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);    // P from TMEM, V MN-major
+      // Descriptors are built once; each k-step adds a compile-time offset (desc_advance).
+      const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 0, 1024);
+      const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 0, 1024);
+      const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), C::CHUNK, 1024);
+      auto issue_s = [&](int t, int j) {                        // S_t = Q_t K_j^T
+        const uint64_t a = desc_advance(dq0, t * C::TILE);
+        const uint64_t b = desc_advance(dk0, (j % C::NS) * C::TILE);
+        const uint32_t d_tmem = tbase + C::T_S + t * 128;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
-          umma_ss(d_tmem, smem_desc_sw128(q_addr + off, 0, 1024),
-                  smem_desc_sw128(k_addr + off, 0, 1024), idesc_s, ks > 0);
+          umma_ss(d_tmem, desc_advance(a, off), desc_advance(b, off), idesc_s, ks > 0);
         }
-        umma_commit(&s_full[j & 1]);
-        umma_commit(&k_empty[s]);
+        umma_commit(&s_full[t]);
       };
-      if (ok && (ok = mbar_wait(&k_full[0], 0, abort_flag, 112))) {
-        tc_fence_after();
-        issue_s(0);
-      }
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        if (j + 1 < n_tiles) {
-          const int s1 = (j + 1) % C::NST;
-          if (!(ok = mbar_wait(&k_full[s1], ((j + 1) / C::NST) & 1, abort_flag, 113))) break;
-          if (j + 1 >= 2 &&
-              !(ok = mbar_wait(&s_free[(j + 1) & 1], (((j + 1) >> 1) - 1) & 1, abort_flag, 114)))
-            break;
-          tc_fence_after();
-          issue_s(j + 1);
-        }
-        const int s = j % C::NST;
-        if (!(ok = mbar_wait(p_full, j & 1, abort_flag, 115))) break;
-        if (!(ok = mbar_wait(&v_full[s], (j / C::NST) & 1, abort_flag, 116))) break;
-        tc_fence_after();
-        const uint32_t v_addr = smem_u32(sV + s * C::TILE);
+      auto issue_pv = [&](int t, int j) {                       // O_t += P_t V_j
+        const uint64_t b = desc_advance(dv0, (j % C::NS) * C::TILE);
+        const uint32_t d_tmem = tbase + C::T_O + t * D;
+        const uint32_t a_tmem = tbase + C::T_S + t * 128;
 #pragma unroll
-        for (int ks = 0; ks < C::BN / 16; ++ks) {
-          const uint32_t a_off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
-          umma_ss(tbase + C::T_O, smem_desc_sw128(p_addr + a_off, 0, 1024),
-                  smem_desc_sw128(v_addr + ks * 2048, C::CHUNK, 1024), idesc_o,
+        for (int ks = 0; ks < C::BN / 16; ++ks)
+          umma_ts(d_tmem, a_tmem + ks * 8, desc_advance(b, ks * 2048), idesc_o,
                   (j > 0 || ks > 0) ? 1u : 0u);
-        }
-        umma_commit(o_done);
-        umma_commit(&v_empty[s]);
+      };
+      bool ok = mbar_wait(q_full, 0, abort_flag, 111) && mbar_wait(&k_full[0], 0, abort_flag, 112);
+      if (ok) {
+        tc_fence_after();
+        if (n_t[0] > 0) issue_s(0, 0);
+        if (n_t[1] > 0) issue_s(1, 0);
+        umma_commit(&k_empty[0]);
       }
-      umma_commit(mma_done);
-      mbar_wait(mma_done, 0, nullptr, 117);
+      for (int j = 0; ok && j < n_max; ++j) {
+        const int s = j % C::NS;
+        if (!(ok = mbar_wait(&v_full[s], (j / C::NS) & 1, abort_flag, 113))) break;
+        bool k_ready = false;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (j < n_t[t]) {
+            if (!(ok = mbar_wait(&p_full[t], j & 1, abort_flag, 115 + t))) break;
+            tc_fence_after();
+            issue_pv(t, j);
+            if (j + 1 == n_t[t]) umma_commit(&o_done[t]);
+          }
+          if (j + 1 < n_t[t]) {
+            if (!k_ready) {
+              if (!(ok = mbar_wait(&k_full[(j + 1) % C::NS], ((j + 1) / C::NS) & 1, abort_flag, 114)))
+                break;
+              tc_fence_after();
+              k_ready = true;
+            }
+            issue_s(t, j + 1);
+          }
+        }
+        if (!ok) break;
+        umma_commit(&v_empty[s]);
+        if (j + 1 < n_max) umma_commit(&k_empty[(j + 1) % C::NS]);
+      }
     }
+  }
   } else {
-    // ------------------------------------------------------------------ softmax warpgroup
+  setmaxnreg_inc<C::REG_SOFTMAX>();   // warpgroups 1 and 2: softmax of query tiles 0 and 1
+  {
+    // ------------------------------------------------------------------ softmax warpgroups
+    const int t = (warp - 4) >> 2;            // query tile of this warpgroup
     const int sub = warp & 3;                 // TMEM lane quarter this warp may access
     const int row = sub * 32 + lane;
     const uint32_t t_lane = static_cast<uint32_t>(sub * 32) << 16;
-    const int q_idx = q0 + row;
+    const uint32_t t_s = tbase + t_lane + C::T_S + t * 128;
+    const uint32_t t_o = tbase + t_lane + C::T_O + t * D;
+    const int q_idx = q0[t] + row;
+    const int n = n_t[t];
     const float c2 = p.scale_log2;
-    float m = -INFINITY;                      // running max of the raw dot products
-    float l = 0.f;                            // running sum, relative to m
+    float m = -INFINITY;                      // reference max (raw dot-product units)
+    float l = 0.f;                            // sum of 2^{(s - m) c2} over keys seen (fp32)
+    float lb = 0.f;                           // the same sum over the bf16-rounded weights
     bool ok = true;
 
-    for (int j = 0; j < n_tiles; ++j) {
-      const int b = j & 1;
-      if (!(ok = mbar_wait_warp(&s_full[b], (j >> 1) & 1, abort_flag, 121))) break;
+    for (int j = 0; j < n; ++j) {
+      if (!(ok = mbar_wait_warp(&s_full[t], j & 1, abort_flag, 121))) break;
       tc_fence_after();
       float s[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int k = 0; k < 4; ++k) {
         uint32_t rr[32];
-        tmem_ld32(tbase + t_lane + C::T_S + b * 128 + c * 32, rr);
-        tmem_wait_ld();
+        tmem_ld32(t_s + k * 32, rr);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(rr[i]);
+        for (int i = 0; i < 32; ++i) s[k * 32 + i] = __uint_as_float(rr[i]);
       }
-      tc_fence_before();
-      mbar_arrive(&s_free[b]);
+      tmem_wait_ld();
 
       const int k0 = j * C::BN;
-      if (k0 + C::BN > p.n_kv || (p.causal && j == qt)) {
+      if (k0 + C::BN > p.n_kv || (p.causal && k0 + C::BN - 1 > q0[t])) {
         const int lim = p.causal ? min(q_idx + 1, p.n_kv) : p.n_kv;   // keys < lim visible
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (k0 + c >= lim) s[c] = -INFINITY;
+        for (int k = 0; k < 128; ++k)
+          if (k0 + k >= lim) s[k] = -INFINITY;
       }
       float mx = s[0];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
-      const float m_new = fmaxf(m, mx);
-      const float ms = (m_new == -INFINITY) ? 0.f : m_new * c2;
-      const float alpha = fast_exp2(m * c2 - ms);       // 0 on the first tile (m = -inf)
-      float rs = 0.f;
-      uint32_t pk[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float p0 = fast_exp2(fmaf(s[2 * c], c2, -ms));
-        const float p1 = fast_exp2(fmaf(s[2 * c + 1], c2, -ms));
-        rs += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
-      }
-      l = l * alpha + rs;
-      m = m_new;
-
-      // PV_{j-1} must be finished before P_j overwrites the P buffer and O is rescaled.
-      if (j > 0) {
-        if (!(ok = mbar_wait_warp(o_done, (j - 1) & 1, abort_flag, 122))) break;
-        tc_fence_after();
-      }
-#pragma unroll
-      for (int c8 = 0; c8 < 16; ++c8) {
-        uint4 v4 = make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
-        *reinterpret_cast<uint4*>(sP + (c8 >> 3) * C::CHUNK + sw128_offset(row, (c8 & 7) * 8)) = v4;
-      }
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t rr[32];
-          const uint32_t ta = tbase + t_lane + C::T_O + c * 32;
-          tmem_ld32(ta, rr);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
-          tmem_st32(ta, rr);
+      for (int k = 1; k < 128; ++k) mx = fmaxf(mx, s[k]);
+      const float cand = fmaxf(m, mx);
+      const bool move = (m == -INFINITY) || ((cand - m) * c2 > C::RESCALE_THRESHOLD);
+      if (__any_sync(0xffffffffu, move)) {
+        const float alpha = move ? fast_exp2((m - cand) * c2) : 1.f;  // 0 when m = -inf
+        if (move) {
+          l *= alpha;
+          lb *= alpha;
+          m = cand;
         }
-        tmem_wait_st();
+        if (j > 0) {
+          // O_t is settled: PV_t(j-1) completed before S_t(j) (same issuing thread, in order).
+#pragma unroll
+          for (int k = 0; k < D / 32; ++k) {
+            uint32_t rr[32];
+            tmem_ld32(t_o + k * 32, rr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+            tmem_st32(t_o + k * 32, rr);
+          }
+        }
       }
-      fence_proxy_async_smem();
+      const float ms = (m == -INFINITY) ? 0.f : m * c2;
+      float rs = 0.f, rb = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {             // P over the first 64 columns of S_t, 2 halves
+        uint32_t pk[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float p0 = fast_exp2(fmaf(s[64 * h + 2 * k], c2, -ms));
+          const float p1 = fast_exp2(fmaf(s[64 * h + 2 * k + 1], c2, -ms));
+          pk[k] = pack_bf16x2(p0, p1);
+          rs += p0 + p1;
+          // lb sums the bf16 weights the PV product uses, so O / lb is an exact weighted
+          // average of V under those weights; lse keeps the fp32 sum
+          rb += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xffff0000u);
+        }
+        tmem_st32(t_s + h * 32, pk);
+      }
+      l += rs;
+      lb += rb;
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[t]);
     }
 
     // ------------------------------------------------------------------ epilogue
-    if (ok && n_tiles > 0) {
-      ok = mbar_wait_warp(o_done, (n_tiles - 1) & 1, abort_flag, 123);
+    if (ok && n > 0) {
+      ok = mbar_wait_warp(&o_done[t], 0, abort_flag, 123);
       tc_fence_after();
     }
-    if (ok) {
-      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+    uint8_t* stage = sQ + t * C::TILE;         // Q_t is dead once o_done[t] fired
+    if (ok && q0[t] < p.n_q) {
+      const float inv_l = (lb > 0.f) ? 1.f / lb : 0.f;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int k = 0; k < D / 32; ++k) {
         uint32_t rr[32];
-        if (n_tiles > 0) {
-          tmem_ld32(tbase + t_lane + C::T_O + c * 32, rr);
+        if (n > 0) {
+          tmem_ld32(t_o + k * 32, rr);
           tmem_wait_ld();
         } else {
 #pragma unroll
@@ -302,8 +342,8 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
           v4.y = pack_bf16x2(__uint_as_float(rr[i + 2]) * inv_l, __uint_as_float(rr[i + 3]) * inv_l);
           v4.z = pack_bf16x2(__uint_as_float(rr[i + 4]) * inv_l, __uint_as_float(rr[i + 5]) * inv_l);
           v4.w = pack_bf16x2(__uint_as_float(rr[i + 6]) * inv_l, __uint_as_float(rr[i + 7]) * inv_l);
-          const int col = c * 32 + i;
-          *reinterpret_cast<uint4*>(sQ + (col >> 6) * C::CHUNK + sw128_offset(row, col & 63)) = v4;
+          const int col = k * 32 + i;
+          *reinterpret_cast<uint4*>(stage + (col >> 6) * C::CHUNK + sw128_offset(row, col & 63)) = v4;
         }
       }
       if (q_idx < p.n_q)
@@ -311,12 +351,13 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
             (l > 0.f) ? fmaf(m, p.scale, logf(l)) : -INFINITY;
       fence_proxy_async_smem();
     }
-    named_bar_sync(1, 128);
-    if (ok && threadIdx.x == 64) {
-      for (int c = 0; c < C::KCH; ++c) tma_store_3d(&p.to, sQ + c * C::CHUNK, c * 64, q0, bh);
+    named_bar_sync(1 + t, 128);
+    if (ok && q0[t] < p.n_q && (threadIdx.x & 127) == 64) {
+      for (int k = 0; k < C::KCH; ++k) tma_store_3d(&p.to, stage + k * C::CHUNK, k * 64, q0[t], bh);
       bulk_commit_group();
       bulk_wait_group_read0();
     }
+  }
   }
 
   __syncwarp();
@@ -344,8 +385,7 @@ static cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   p.lse = a.lse;
   p.n_q = a.n_q;
   p.n_kv = a.n_kv;
-  p.bh = static_cast<int>(bh);
-  p.n_qtiles = (a.n_q + C::BM - 1) / C::BM;
+  p.n_qpairs = (a.n_q + 2 * C::BM - 1) / (2 * C::BM);
   p.n_kvtiles = (a.n_kv + C::BN - 1) / C::BN;
   p.causal = a.causal;
   p.scale = a.scale;
@@ -353,7 +393,7 @@ static cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   static int attr_done[64] = {0};   // one per instantiation of this launcher
   cudaError_t e = ensure_smem_attr(fwd_kernel<D>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
-  const uint64_t grid = static_cast<uint64_t>(p.n_qtiles) * bh;
+  const uint64_t grid = static_cast<uint64_t>(p.n_qpairs) * bh;
   fwd_kernel<D><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }

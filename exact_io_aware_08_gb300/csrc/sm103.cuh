@@ -57,6 +57,17 @@ __device__ __forceinline__ uint32_t elect_one_sync() {
   return pred;
 }
 
+// Per-warpgroup register budget (warpgroup-collective).  The sum over warpgroups after the
+// changes must not exceed what the CTA was launched with, or the increase waits forever.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(N));
+}
+
 // ------------------------------------------------------------------------------------------
 // mbarrier
 // ------------------------------------------------------------------------------------------
@@ -203,6 +214,18 @@ __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64
       :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]: A (M x K, bf16) read from tensor memory, row m on lane m,
+// two consecutive K elements per 32-bit column (lower K in the low half), so one K=16 step
+// covers 8 columns.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "setp.ne.b32 P, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, P;\n\t}"
+      :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
 // Arrive once on ``bar`` when all previously issued tcgen05.mma of this thread complete.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
@@ -275,6 +298,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   d |= static_cast<uint64_t>(1) << 46;   // descriptor version for tcgen05
   d |= static_cast<uint64_t>(2) << 61;   // swizzle mode: 128 B
   return d;
+}
+
+// Move a shared-memory descriptor's start address by ``bytes`` (a multiple of 16).  Only the
+// 14-bit start field changes: shared-memory addresses / 16 stay below 2^14, so no carry leaves
+// the field.  With compile-time ``bytes`` this is a single add per MMA.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) {
+  return desc + static_cast<uint64_t>(bytes >> 4);
 }
 
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 accumulation.
