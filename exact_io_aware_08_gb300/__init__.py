@@ -16,7 +16,7 @@ import threading
 
 __all__ = [
     "FaError", "load_library", "library_path",
-    "fa_fwd", "fa_bwd", "fa_bwd_prep", "fa_bwd_main", "fa_bwd_finish", "fa_decode_splitkv", "fa_bwd_workspace_size",
+    "fa_fwd", "fa_bwd", "fa_bwd_prep", "fa_bwd_main", "fa_bwd_finish", "fa_decode_splitkv", "fa_bwd_workspace_size", "fa_decode_splitkv_noalloc",
     "fa_decode_workspace_size", "fa_sync_status", "fa_status_string", "fa_last_error_message",
     "forward", "backward", "decode",
 ]
@@ -55,6 +55,7 @@ _SIGNATURES = {
     "fa_bwd_finish": (_I, [_P, _P, _S, _I, _I, _I, _I, _I, _F, _P]),
     "fa_decode_workspace_size": (_S, [_I, _I, _I, _I, _I]),
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
+    "fa_decode_splitkv_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_sync_status": (_I, [_P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_last_error_message": (ctypes.c_char_p, []),
@@ -159,6 +160,16 @@ def fa_decode_splitkv(q, k, v, o, lse, scale: float, n_splits: int, ws, stream=N
     _check(load_library().fa_decode_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, n_kv,
                                             d, float(scale), int(n_splits), _ptr(ws), ws_bytes,
                                             _stream(stream)))
+
+
+def fa_decode_splitkv_noalloc(q, k, v, o, lse, scale: float, n_splits: int, stream=None):
+    """Split-KV decode without a workspace: the library keeps the per-chunk states in a fixed
+    device array of FA_DECODE_NOALLOC_SCRATCH_BYTES (see include/fa.h for the limit and the
+    rule that overlapping calls race on it)."""
+    B, H, _, d = q.shape
+    _check(load_library().fa_decode_splitkv_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H,
+                                                    k.shape[2], d, float(scale), int(n_splits),
+                                                    _stream(stream)))
 
 
 def fa_sync_status(stream=None):

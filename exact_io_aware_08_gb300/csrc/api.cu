@@ -216,6 +216,37 @@ fa_status_t fa_decode_splitkv(const fa_bf16_t* q, const fa_bf16_t* k, const fa_b
   return FA_OK;
 }
 
+fa_status_t fa_decode_splitkv_noalloc(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
+                                      fa_bf16_t* o, float* lse, int B, int H, int N_kv, int d,
+                                      float scale, int n_splits, void* stream) {
+  fa_status_t st = check_shape(B, H, 1, N_kv, d, scale);
+  if (st != FA_OK) return st;
+  if (n_splits > fa::kDecodeMaxSplits)
+    return fail(FA_ERR_UNSUPPORTED, "n_splits=%d exceeds %d", n_splits, fa::kDecodeMaxSplits);
+  if (n_splits <= 0) n_splits = fa::decode_auto_splits(B, H, N_kv);
+  if (!q || !o || !lse || (N_kv > 0 && (!k || !v)))
+    return fail(FA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(FA_ERR_INVALID_ARG, "arrays must be 16-byte aligned");
+  const size_t need = fa::decode_part_bytes(B, H, d, n_splits);
+  if (need > fa::kDecodeNoallocScratchBytes)
+    return fail(FA_ERR_UNSUPPORTED,
+                "fa_decode_splitkv_noalloc: B*H*n_splits*(d+2)*4 = %zu bytes exceeds the fixed "
+                "scratch of %zu bytes; use fa_decode_splitkv with a workspace or fewer splits",
+                need, fa::kDecodeNoallocScratchBytes);
+  float* scratch = nullptr;
+  cudaError_t e = fa::decode_noalloc_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_decode_splitkv_noalloc scratch lookup");
+  fa::DecodeArgs a{};
+  a.q = q; a.k = N_kv ? k : q; a.v = N_kv ? v : q; a.o = o; a.lse = lse;
+  a.part = scratch;
+  a.B = B; a.H = H; a.n_kv = N_kv; a.d = d; a.scale = scale; a.n_splits = n_splits;
+  a.chunk = fa::decode_chunk(N_kv, n_splits);
+  e = fa::launch_decode(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_decode_splitkv_noalloc launch");
+  return FA_OK;
+}
+
 fa_status_t fa_sync_status(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned int code = 0, c = 0;

@@ -320,6 +320,35 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   return launch_decode_d<128>(a, stream);
 }
 
+// ------------------------------------------------------------------------------------------
+// Fixed scratch for fa_decode_splitkv_noalloc: the per-chunk states live in this array instead
+// of a caller workspace.  It is part of the library image, so every GPU that loads the library
+// holds it until the process exits.  Host code must not pass the symbol itself to a kernel
+// (on the host it names a stand-in, not device memory): decode_noalloc_scratch() looks up the
+// device address once per device with that device current.
+// ------------------------------------------------------------------------------------------
+static __device__ __align__(256) float g_decode_scratch[kDecodeNoallocScratchBytes / sizeof(float)];
+
+cudaError_t decode_noalloc_scratch(float** ptr) {
+  static float* cached[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64) {
+    float* c = __atomic_load_n(&cached[dev], __ATOMIC_ACQUIRE);
+    if (c) {
+      *ptr = c;
+      return cudaSuccess;
+    }
+  }
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_decode_scratch);
+  if (e != cudaSuccess) return e;
+  if (dev < 64) __atomic_store_n(&cached[dev], static_cast<float*>(p), __ATOMIC_RELEASE);
+  *ptr = static_cast<float*>(p);
+  return cudaSuccess;
+}
+
 }  // namespace fa
 
 FA_DEFINE_STATUS_FETCH(status_fetch_decode)

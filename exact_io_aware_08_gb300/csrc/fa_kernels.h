@@ -100,6 +100,11 @@ inline size_t decode_part_bytes(int B, int H, int d, int n_splits) {
   return static_cast<size_t>(B) * H * n_splits * (d + 2) * sizeof(float);
 }
 
+// Size of the fixed device scratch behind fa_decode_splitkv_noalloc (decode.cu).
+constexpr size_t kDecodeNoallocScratchBytes = size_t(8) << 20;
+// Device address of that scratch on the current device (looked up once per device).
+cudaError_t decode_noalloc_scratch(float** ptr);
+
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (kernel, device).  ``done`` is a
 // per-kernel flag array owned by the caller (kernels of the same signature must not share one).
 template <typename F>

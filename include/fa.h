@@ -137,6 +137,33 @@ fa_status_t fa_decode_splitkv(const fa_bf16_t* q, const fa_bf16_t* k, const fa_b
                               void* stream);
 
 /*
+ * fa_decode_splitkv_noalloc -- fa_decode_splitkv for callers that cannot allocate device
+ * memory (no counterpart in the pages; an interface convenience).
+ *
+ * Some callers have no way to hand the decode a workspace: a plugin inside a host process
+ * whose memory manager owns all device memory, or a latency-critical serving loop that must
+ * not call cudaMalloc (which can synchronise the device).  This entry point computes exactly
+ * what fa_decode_splitkv computes, with the same kernels, but keeps the per-chunk states in a
+ * fixed scratch array compiled into the library (FA_DECODE_NOALLOC_SCRATCH_BYTES of device
+ * memory, held on every GPU that loads the library until the process exits).  It never calls
+ * cudaMalloc, cudaFree or any allocating routine.
+ *
+ *  - Arguments are those of fa_decode_splitkv without ws/ws_bytes.
+ *  - Limit: B * H * n_splits * (d + 2) * 4 bytes must not exceed the scratch size (for the
+ *    automatic n_splits the library's choice is checked); larger calls return
+ *    FA_ERR_UNSUPPORTED before anything is launched.
+ *  - The first call on a device looks up the scratch's device address (cudaGetSymbolAddress)
+ *    with that device current; make that first call before any stream capture.
+ *  - Every call shares the one array and leaves its contents behind.  Nothing in it needs to
+ *    start at zero (each call writes every state it reads), but two calls whose kernels overlap
+ *    on the GPU (different streams, or different host threads) race on it: serialise them.
+ */
+#define FA_DECODE_NOALLOC_SCRATCH_BYTES (8u << 20)
+fa_status_t fa_decode_splitkv_noalloc(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
+                                      fa_bf16_t* o, float* lse, int B, int H, int N_kv, int d,
+                                      float scale, int n_splits, void* stream);
+
+/*
  * fa_sync_status -- synchronise ``stream`` and report device-side failures recorded by any
  * kernel of this library since the last call (currently: a bounded pipeline wait that ran
  * out, FA_ERR_DEVICE_TIMEOUT).  Clears the recorded state.  Also returns FA_ERR_CUDA if the
