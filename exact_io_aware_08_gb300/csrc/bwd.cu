@@ -198,21 +198,28 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0 && n > 0) {
-      const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
-      const uint32_t pt_addr = smem_u32(sPT), ds_addr = smem_u32(sDS);
       const uint32_t id_s = idesc_bf16_f32(128, C::BM, 0, 0);     // K/V K-major, Q/dO K-major
       const uint32_t id_acc = idesc_bf16_f32(128, D, 0, 1);       // P^T/dS^T K-major, dO/Q MN-major
       const uint32_t id_dq = idesc_bf16_f32(128, 64, 1, 1);       // both MN-major
+      // Descriptors are built once; every k-step adds a compile-time offset (desc_advance).
+      const uint64_t dK_k = smem_desc_sw128(smem_u32(sK), 0, 1024);          // K as K-major A
+      const uint64_t dV_k = smem_desc_sw128(smem_u32(sV), 0, 1024);          // V as K-major A
+      const uint64_t dK_mn = smem_desc_sw128(smem_u32(sK), C::KV_CHUNK, 1024);  // K as MN-major
+      const uint64_t dPT = smem_desc_sw128(smem_u32(sPT), 0, 1024);
+      const uint64_t dDS = smem_desc_sw128(smem_u32(sDS), 0, 1024);
+      const uint64_t dDS_mn = smem_desc_sw128(smem_u32(sDS), C::KV_CHUNK, 1024);
+      const uint64_t dST_k = smem_desc_sw128(smem_u32(stage_ptr(0)), 0, 1024);        // Q/dO K-major
+      const uint64_t dST_mn = smem_desc_sw128(smem_u32(stage_ptr(0)), C::Q_CHUNK, 1024);  // MN-major
       auto issue_s_dp = [&](int i) {
-        const uint32_t st = smem_u32(stage_ptr(i % C::NST));
+        const uint32_t st = (i % C::NST) * C::STAGE;
+        const uint64_t q_k = desc_advance(dST_k, st);
+        const uint64_t do_k = desc_advance(dST_k, st + C::Q_TILE);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t kv_off = (ks >> 2) * C::KV_CHUNK + (ks & 3) * 32;
           const uint32_t q_off = (ks >> 2) * C::Q_CHUNK + (ks & 3) * 32;
-          umma_ss(tbase + C::T_S, smem_desc_sw128(k_addr + kv_off, 0, 1024),
-                  smem_desc_sw128(st + q_off, 0, 1024), id_s, ks > 0);
-          umma_ss(tbase + C::T_DP, smem_desc_sw128(v_addr + kv_off, 0, 1024),
-                  smem_desc_sw128(st + C::Q_TILE + q_off, 0, 1024), id_s, ks > 0);
+          umma_ss(tbase + C::T_S, desc_advance(dK_k, kv_off), desc_advance(q_k, q_off), id_s, ks > 0);
+          umma_ss(tbase + C::T_DP, desc_advance(dV_k, kv_off), desc_advance(do_k, q_off), id_s, ks > 0);
         }
         umma_commit(st_full);
       };
@@ -233,17 +240,16 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
         }
         if (!(ok = mbar_wait(pds_ready, i & 1, abort_flag, 215))) break;
         tc_fence_after();
-        const uint32_t st = smem_u32(stage_ptr(s));
+        const uint64_t q_mn = desc_advance(dST_mn, s * C::STAGE);
+        const uint64_t do_mn = desc_advance(dST_mn, s * C::STAGE + C::Q_TILE);
 #pragma unroll
         for (int ks = 0; ks < C::BM / 16; ++ks) {
           const uint32_t a_off = (ks >> 2) * C::KV_CHUNK + (ks & 3) * 32;
           const uint32_t acc = (i > 0 || ks > 0) ? 1u : 0u;
           // dV += P^T dO
-          umma_ss(tbase + C::T_DV, smem_desc_sw128(pt_addr + a_off, 0, 1024),
-                  smem_desc_sw128(st + C::Q_TILE + ks * 2048, C::Q_CHUNK, 1024), id_acc, acc);
+          umma_ss(tbase + C::T_DV, desc_advance(dPT, a_off), desc_advance(do_mn, ks * 2048), id_acc, acc);
           // dK += dS^T Q
-          umma_ss(tbase + C::T_DK, smem_desc_sw128(ds_addr + a_off, 0, 1024),
-                  smem_desc_sw128(st + ks * 2048, C::Q_CHUNK, 1024), id_acc, acc);
+          umma_ss(tbase + C::T_DK, desc_advance(dDS, a_off), desc_advance(q_mn, ks * 2048), id_acc, acc);
         }
         const int qb = i & 1;                    // dQ TMEM buffer of this step
         if (i >= 2) {
@@ -254,8 +260,8 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
         for (int ks = 0; ks < C::BN / 16; ++ks) {
           // d = 128: dQ^T = K^T dS^T (A = K as MN-major, B = dS^T as MN-major)
           // d = 64:  dQ   = dS K     (A = dS^T as MN-major, B = K as MN-major)
-          const uint64_t kd = smem_desc_sw128(k_addr + ks * 2048, C::KV_CHUNK, 1024);
-          const uint64_t dd = smem_desc_sw128(ds_addr + ks * 2048, C::KV_CHUNK, 1024);
+          const uint64_t kd = desc_advance(dK_mn, ks * 2048);
+          const uint64_t dd = desc_advance(dDS_mn, ks * 2048);
           if constexpr (D == 128) umma_ss(tbase + C::T_DQ + qb * 64, kd, dd, id_dq, ks > 0);
           else umma_ss(tbase + C::T_DQ + qb * 64, dd, kd, id_dq, ks > 0);
         }
