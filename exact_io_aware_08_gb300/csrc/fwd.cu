@@ -268,9 +268,16 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
         for (int k = 0; k < 128; ++k)
           if (k0 + k >= lim) s[k] = -INFINITY;
       }
-      float mx = s[0];
+      // row max: four independent 3-input-max chains, then combined
+      float mq[4];
 #pragma unroll
-      for (int k = 1; k < 128; ++k) mx = fmaxf(mx, s[k]);
+      for (int g = 0; g < 4; ++g) {
+        mq[g] = fmax3(s[32 * g], s[32 * g + 1], s[32 * g + 2]);
+#pragma unroll
+        for (int k = 3; k < 31; k += 2) mq[g] = fmax3(mq[g], s[32 * g + k], s[32 * g + k + 1]);
+        mq[g] = fmaxf(mq[g], s[32 * g + 31]);
+      }
+      const float mx = fmaxf(fmax3(mq[0], mq[1], mq[2]), mq[3]);
       const float cand = fmaxf(m, mx);
       const bool move = (m == -INFINITY) || ((cand - m) * c2 > C::RESCALE_THRESHOLD);
       if (__any_sync(0xffffffffu, move)) {
@@ -288,30 +295,42 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
             tmem_ld32(t_o + k * 32, rr);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+            for (int i = 0; i < 32; i += 2) {
+              const float2 v = fmul2(make_float2(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1])),
+                                     make_float2(alpha, alpha));
+              rr[i] = __float_as_uint(v.x);
+              rr[i + 1] = __float_as_uint(v.y);
+            }
             tmem_st32(t_o + k * 32, rr);
           }
         }
       }
       const float ms = (m == -INFINITY) ? 0.f : m * c2;
-      float rs = 0.f, rb = 0.f;
+      const float2 c2v = make_float2(c2, c2), nms = make_float2(-ms, -ms);
+      float2 rs[4], rb[4];                      // independent partial sums (ILP)
+#pragma unroll
+      for (int g = 0; g < 4; ++g) rs[g] = rb[g] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {             // P over the first 64 columns of S_t, 2 halves
         uint32_t pk[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const float p0 = fast_exp2(fmaf(s[64 * h + 2 * k], c2, -ms));
-          const float p1 = fast_exp2(fmaf(s[64 * h + 2 * k + 1], c2, -ms));
+          const float2 x = ffma2(make_float2(s[64 * h + 2 * k], s[64 * h + 2 * k + 1]), c2v, nms);
+          const float p0 = fast_exp2(x.x);
+          const float p1 = fast_exp2(x.y);
           pk[k] = pack_bf16x2(p0, p1);
-          rs += p0 + p1;
+          rs[k & 3] = fadd2(rs[k & 3], make_float2(p0, p1));
           // lb sums the bf16 weights the PV product uses, so O / lb is an exact weighted
           // average of V under those weights; lse keeps the fp32 sum
-          rb += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xffff0000u);
+          rb[k & 3] = fadd2(rb[k & 3], make_float2(__uint_as_float(pk[k] << 16),
+                                                   __uint_as_float(pk[k] & 0xffff0000u)));
         }
         tmem_st32(t_s + h * 32, pk);
       }
-      l += rs;
-      lb += rb;
+      const float2 rs01 = fadd2(fadd2(rs[0], rs[1]), fadd2(rs[2], rs[3]));
+      const float2 rb01 = fadd2(fadd2(rb[0], rb[1]), fadd2(rb[2], rb[3]));
+      l += rs01.x + rs01.y;
+      lb += rb01.x + rb01.y;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(&p_full[t]);
