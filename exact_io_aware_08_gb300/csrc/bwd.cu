@@ -14,11 +14,13 @@
 //         warp 0     TMA producer: K_j, V_j once; Q_i, dO_i (+ lse_i, D_i) per query tile
 //                    through a 3-deep ring.
 //         warp 1     TMEM owner and MMA issuer: S^T = K Q^T, dP^T = V dO^T (keys on TMEM
-//                    lanes), dV += P^T dO, dK += dS^T Q, and the dQ tile product.
+//                    lanes), dV += P^T dO (P^T read from TMEM), dK += dS^T Q, and the dQ tile
+//                    product, issued per step as dV_i, S/dP_{i+1}, dK_i, dQ_i.
 //         warps 2-9  two warpgroups, thread = (key row, half of the query columns):
-//                    P^T = 2^{S^T scale log2e - lse log2e} (masked), dS^T = P^T o (dP^T - D),
-//                    both written as bf16 to shared memory as MMA operands.  Epilogue: one
-//                    group writes dV, the other dK (times scale), through TMA stores.
+//                    P^T = 2^{S^T scale log2e - lse log2e} (masked), dS^T = P^T o (dP^T - D).
+//                    P^T (bf16) goes back into TMEM over the S^T columns just read; dS^T
+//                    (bf16) goes to shared memory, where the dK and dQ products read it.
+//                    Epilogue: one group writes dV, the other dK (times scale), via TMA.
 //         warps 10-13 drain the dQ tile from TMEM into the fp32 accumulator with vector
 //                    reductions (red.global.add), overlapping the next tile's MMAs.
 //       TMEM (512 columns): dV, dK (d each), S^T, dP^T (BM each), two dQ tiles (64 each), so
@@ -43,18 +45,17 @@ struct BwdCfg {
   static constexpr int KV_CHUNK = BN * 128;         // [128 rows x 64 cols] swizzled
   static constexpr int Q_TILE = BM * D * 2;
   static constexpr int Q_CHUNK = BM * 128;          // [BM rows x 64 cols] swizzled
-  static constexpr int PT_TILE = BN * BM * 2;       // P^T or dS^T, [QCH][128][64]
+  static constexpr int DS_TILE = BN * BM * 2;       // dS^T, [QCH][128][64]
   static constexpr int NST = 3;
   static constexpr int STAGE = 2 * Q_TILE + 1024;   // Q, dO, then lse2[BM], delta[BM]
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = KV_TILE;
   static constexpr int OFF_ST = 2 * KV_TILE;
-  static constexpr int OFF_PT = OFF_ST + NST * STAGE;
-  static constexpr int OFF_DS = OFF_PT + PT_TILE;
-  static constexpr int OFF_BAR = OFF_DS + PT_TILE;
-  // kv_full, stage_full[NST], stage_empty[NST], st_full, st_free, pds_ready, pds_free,
+  static constexpr int OFF_DS = OFF_ST + NST * STAGE;
+  static constexpr int OFF_BAR = OFF_DS + DS_TILE;
+  // kv_full, stage_full[NST], stage_empty[NST], st_full, pds_ready, pds_free,
   // dq_full[2], dq_free[2], mma_done
-  static constexpr int NBAR = 1 + 2 * NST + 9;
+  static constexpr int NBAR = 1 + 2 * NST + 8;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -95,15 +96,13 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
   uint8_t* smem = align_smem_1k(smem_raw);
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
-  uint8_t* sPT = smem + C::OFF_PT;
   uint8_t* sDS = smem + C::OFF_DS;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* kv_full = bars;
   uint64_t* stage_full = bars + 1;
   uint64_t* stage_empty = stage_full + C::NST;
   uint64_t* st_full = stage_empty + C::NST;
-  uint64_t* st_free = st_full + 1;
-  uint64_t* pds_ready = st_free + 1;
+  uint64_t* pds_ready = st_full + 1;
   uint64_t* pds_free = pds_ready + 1;
   uint64_t* dq_full = pds_free + 1;      // [2], one per dQ TMEM buffer
   uint64_t* dq_free = dq_full + 2;       // [2]
@@ -130,7 +129,6 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       mbar_init(&stage_empty[s], 1);
     }
     mbar_init(st_full, 1);
-    mbar_init(st_free, C::DS_THREADS);
     mbar_init(pds_ready, C::DS_THREADS);
     mbar_init(pds_free, 1);
     for (int b2 = 0; b2 < 2; ++b2) {
@@ -182,8 +180,8 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
         const size_t rowbase = static_cast<size_t>(bh) * p.n_q;
         for (int e = lane; e < C::BM; e += 32) {
           const int q = q0 + e;
-          s_lse[e] = (q < p.n_q) ? p.lse[rowbase + q] * 1.4426950408889634f : INFINITY;
-          s_del[e] = (q < p.n_q) ? p.delta[rowbase + q] : 0.f;
+          s_lse[e] = (q < p.n_q) ? -p.lse[rowbase + q] * 1.4426950408889634f : -INFINITY;
+          s_del[e] = (q < p.n_q) ? -p.delta[rowbase + q] : 0.f;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&stage_full[s]);
@@ -199,13 +197,12 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0 && n > 0) {
       const uint32_t id_s = idesc_bf16_f32(128, C::BM, 0, 0);     // K/V K-major, Q/dO K-major
-      const uint32_t id_acc = idesc_bf16_f32(128, D, 0, 1);       // P^T/dS^T K-major, dO/Q MN-major
+      const uint32_t id_acc = idesc_bf16_f32(128, D, 0, 1);       // P^T (TMEM) / dS^T K-major, dO/Q MN-major
       const uint32_t id_dq = idesc_bf16_f32(128, 64, 1, 1);       // both MN-major
       // Descriptors are built once; every k-step adds a compile-time offset (desc_advance).
       const uint64_t dK_k = smem_desc_sw128(smem_u32(sK), 0, 1024);          // K as K-major A
       const uint64_t dV_k = smem_desc_sw128(smem_u32(sV), 0, 1024);          // V as K-major A
       const uint64_t dK_mn = smem_desc_sw128(smem_u32(sK), C::KV_CHUNK, 1024);  // K as MN-major
-      const uint64_t dPT = smem_desc_sw128(smem_u32(sPT), 0, 1024);
       const uint64_t dDS = smem_desc_sw128(smem_u32(sDS), 0, 1024);
       const uint64_t dDS_mn = smem_desc_sw128(smem_u32(sDS), C::KV_CHUNK, 1024);
       const uint64_t dST_k = smem_desc_sw128(smem_u32(stage_ptr(0)), 0, 1024);        // Q/dO K-major
@@ -229,27 +226,29 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
         tc_fence_after();
         issue_s_dp(0);
       }
+      // Per step i: dV_i (P^T from TMEM, over the S^T columns), then S/dP of step i+1 (they
+      // overwrite those columns, so they come after dV_i in issue order), then dK_i and dQ_i.
       for (int i = 0; ok && i < n; ++i) {
         const int s = i % C::NST;
-        if (i + 1 < n) {
-          if (!(ok = mbar_wait(st_free, i & 1, abort_flag, 213))) break;
-          if (!(ok = mbar_wait(&stage_full[(i + 1) % C::NST], ((i + 1) / C::NST) & 1, abort_flag, 214)))
-            break;
-          tc_fence_after();
-          issue_s_dp(i + 1);
-        }
         if (!(ok = mbar_wait(pds_ready, i & 1, abort_flag, 215))) break;
         tc_fence_after();
         const uint64_t q_mn = desc_advance(dST_mn, s * C::STAGE);
         const uint64_t do_mn = desc_advance(dST_mn, s * C::STAGE + C::Q_TILE);
 #pragma unroll
-        for (int ks = 0; ks < C::BM / 16; ++ks) {
+        for (int ks = 0; ks < C::BM / 16; ++ks)       // dV += P^T dO
+          umma_ts(tbase + C::T_DV, tbase + C::T_S + ks * 8 + ((16 * ks) / C::HALF) * (C::HALF / 2),
+                  desc_advance(do_mn, ks * 2048), id_acc, (i > 0 || ks > 0) ? 1u : 0u);
+        if (i + 1 < n) {
+          if (!(ok = mbar_wait(&stage_full[(i + 1) % C::NST], ((i + 1) / C::NST) & 1, abort_flag, 214)))
+            break;
+          tc_fence_after();
+          issue_s_dp(i + 1);
+        }
+#pragma unroll
+        for (int ks = 0; ks < C::BM / 16; ++ks) {     // dK += dS^T Q
           const uint32_t a_off = (ks >> 2) * C::KV_CHUNK + (ks & 3) * 32;
-          const uint32_t acc = (i > 0 || ks > 0) ? 1u : 0u;
-          // dV += P^T dO
-          umma_ss(tbase + C::T_DV, desc_advance(dPT, a_off), desc_advance(do_mn, ks * 2048), id_acc, acc);
-          // dK += dS^T Q
-          umma_ss(tbase + C::T_DK, desc_advance(dDS, a_off), desc_advance(q_mn, ks * 2048), id_acc, acc);
+          umma_ss(tbase + C::T_DK, desc_advance(dDS, a_off), desc_advance(q_mn, ks * 2048), id_acc,
+                  (i > 0 || ks > 0) ? 1u : 0u);
         }
         const int qb = i & 1;                    // dQ TMEM buffer of this step
         if (i >= 2) {
@@ -289,52 +288,55 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       // lse/D of this stage were written by the producer warp: acquire them directly
       if (!(ok = mbar_wait_warp(&stage_full[i % C::NST], (i / C::NST) & 1, abort_flag, 224))) break;
       tc_fence_after();
-      const float* s_lse = reinterpret_cast<const float*>(stage_ptr(i % C::NST) + 2 * C::Q_TILE);
-      const float* s_del = s_lse + C::BM;
+      const float* s_nlse = reinterpret_cast<const float*>(stage_ptr(i % C::NST) + 2 * C::Q_TILE);
+      const float* s_nd = s_nlse + C::BM;
       const bool diag = p.causal && (q0 < k0 + C::BN - 1);
-      uint32_t pk_p[C::HALF / 2], pk_ds[C::HALF / 2];
+      const float2 c2v = make_float2(c2, c2);
+      uint32_t pk_ds[C::HALF / 2];
 #pragma unroll
       for (int c = 0; c < C::HALF / 32; ++c) {
         uint32_t rs[32], rd[32];
         tmem_ld32(tbase + t_lane + C::T_S + cb + c * 32, rs);
         tmem_ld32(tbase + t_lane + C::T_DP + cb + c * 32, rd);
-        // per-column lse (log2 units) and D: the same for every thread, read as broadcasts
-        float lv[32], dl[32];
+        // per-column -lse (log2 units) and -D: the same for every thread (broadcast reads)
+        float nl[32], nd[32];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          const float4 a = *reinterpret_cast<const float4*>(s_lse + cb + c * 32 + e);
-          const float4 b4 = *reinterpret_cast<const float4*>(s_del + cb + c * 32 + e);
-          lv[e] = a.x; lv[e + 1] = a.y; lv[e + 2] = a.z; lv[e + 3] = a.w;
-          dl[e] = b4.x; dl[e + 1] = b4.y; dl[e + 2] = b4.z; dl[e + 3] = b4.w;
+          const float4 a = *reinterpret_cast<const float4*>(s_nlse + cb + c * 32 + e);
+          const float4 b4 = *reinterpret_cast<const float4*>(s_nd + cb + c * 32 + e);
+          nl[e] = a.x; nl[e + 1] = a.y; nl[e + 2] = a.z; nl[e + 3] = a.w;
+          nd[e] = b4.x; nd[e + 1] = b4.y; nd[e + 2] = b4.z; nd[e + 3] = b4.w;
         }
         tmem_wait_ld();
-        float pv[32], dsv[32];
+        uint32_t pk_p[16];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
+        for (int e = 0; e < 32; e += 2) {
           const int col = cb + c * 32 + e;
-          float pe = fast_exp2(fmaf(__uint_as_float(rs[e]), c2, -lv[e]));
-          if (row_dead || (diag && k_idx > q0 + col)) pe = 0.f;
-          pv[e] = pe;
-          dsv[e] = pe * (__uint_as_float(rd[e]) - dl[e]);
+          const float2 x = ffma2(make_float2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2v,
+                                 make_float2(nl[e], nl[e + 1]));
+          float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+          if (row_dead || (diag && k_idx > q0 + col)) p0 = 0.f;
+          if (row_dead || (diag && k_idx > q0 + col + 1)) p1 = 0.f;
+          const float2 ds = fmul2(make_float2(p0, p1),
+                                  fadd2(make_float2(__uint_as_float(rd[e]), __uint_as_float(rd[e + 1])),
+                                        make_float2(nd[e], nd[e + 1])));
+          pk_p[e / 2] = pack_bf16x2(p0, p1);
+          pk_ds[c * 16 + e / 2] = pack_bf16x2(ds.x, ds.y);
         }
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          pk_p[c * 16 + e] = pack_bf16x2(pv[2 * e], pv[2 * e + 1]);
-          pk_ds[c * 16 + e] = pack_bf16x2(dsv[2 * e], dsv[2 * e + 1]);
-        }
+        // P^T goes back over S^T columns this thread has already read (its own half, bf16 pairs):
+        // group g's query q sits at column g*HALF + (q - g*HALF)/2, where the dV product reads it
+        tmem_st16(tbase + t_lane + C::T_S + cb + c * 16, pk_p);
       }
-      tc_fence_before();
-      mbar_arrive(st_free);
       if (i > 0 && !(ok = mbar_wait_warp(pds_free, (i - 1) & 1, abort_flag, 222))) break;
 #pragma unroll
       for (int u = 0; u < C::HALF / 8; ++u) {
         const int c8 = cb / 8 + u;                   // 16-byte unit along the query axis
         const uint32_t off = (c8 >> 3) * C::KV_CHUNK + sw128_offset(r, (c8 & 7) * 8);
-        *reinterpret_cast<uint4*>(sPT + off) =
-            make_uint4(pk_p[4 * u], pk_p[4 * u + 1], pk_p[4 * u + 2], pk_p[4 * u + 3]);
         *reinterpret_cast<uint4*>(sDS + off) =
             make_uint4(pk_ds[4 * u], pk_ds[4 * u + 1], pk_ds[4 * u + 2], pk_ds[4 * u + 3]);
       }
+      tmem_wait_st();
+      tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(pds_ready);
     }
