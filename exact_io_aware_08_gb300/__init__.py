@@ -57,6 +57,7 @@ _SIGNATURES = {
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
     "fa_decode_splitkv_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_sync_status": (_I, [_P]),
+    "fa_selftest_wait_timeout": (_I, [ctypes.c_uint, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_last_error_message": (ctypes.c_char_p, []),
 }
@@ -174,6 +175,11 @@ def fa_decode_splitkv_noalloc(q, k, v, o, lse, scale: float, n_splits: int, stre
 
 def fa_sync_status(stream=None):
     _check(load_library().fa_sync_status(_stream(stream)))
+
+
+def fa_selftest_wait_timeout(limit_us: int, stream=None):
+    """Enqueue the diagnostic bounded wait (see include/fa.h); check it with fa_sync_status()."""
+    _check(load_library().fa_selftest_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def fa_status_string(status: int) -> str:

@@ -247,12 +247,22 @@ fa_status_t fa_decode_splitkv_noalloc(const fa_bf16_t* q, const fa_bf16_t* k, co
   return FA_OK;
 }
 
+fa_status_t fa_selftest_wait_timeout(unsigned int limit_us, void* stream) {
+  if (limit_us == 0 || limit_us > 10u * 1000u * 1000u)
+    return fail(FA_ERR_INVALID_ARG, "limit_us must be in [1, 10000000] (got %u)", limit_us);
+  cudaError_t e = fa::launch_selftest_wait(static_cast<unsigned long long>(limit_us) * 1000ull,
+                                           static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_selftest_wait_timeout launch");
+  return FA_OK;
+}
+
 fa_status_t fa_sync_status(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned int code = 0, c = 0;
   int where = 0, w = 0;
   cudaError_t (*fetch[])(cudaStream_t, unsigned int*, int*) = {
-      fa::status_fetch_fwd, fa::status_fetch_bwd, fa::status_fetch_decode};
+      fa::status_fetch_fwd, fa::status_fetch_bwd, fa::status_fetch_decode,
+      fa::status_fetch_selftest};
   for (auto f : fetch) {
     cudaError_t e = f(s, &c, &w);
     if (e != cudaSuccess) return cuda_fail(e, "fa_sync_status");

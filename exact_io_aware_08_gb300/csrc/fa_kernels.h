@@ -67,6 +67,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t status_fetch_fwd(cudaStream_t, unsigned int*, int*);
 cudaError_t status_fetch_bwd(cudaStream_t, unsigned int*, int*);
 cudaError_t status_fetch_decode(cudaStream_t, unsigned int*, int*);
+cudaError_t status_fetch_selftest(cudaStream_t, unsigned int*, int*);
+
+// Diagnostic kernel: a bounded wait that is never satisfied (selftest.cu).
+cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream);
 
 // Workspace layout of the backward pass.
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

@@ -107,22 +107,28 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Bounded wait for the phase with the given parity.  Returns true on completion, false when the
 // limit ran out or another role of this CTA already aborted (``abort_flag`` in shared memory).
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort_flag, int where) {
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity,
+                                                volatile int* abort_flag, int where,
+                                                uint64_t limit_ns) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(a, parity)) return true;
-    if ((it & 255u) == 0) {
+    if ((it & 15u) == 0) {
       if (abort_flag && *abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         report_device_error(FA_DEV_TIMEOUT, where);
         if (abort_flag) *abort_flag = 1;
         return false;
       }
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          volatile int* abort_flag, int where) {
+  return mbar_wait_limit(bar, parity, abort_flag, where, kWaitLimitNs);
 }
 
 // Warp-uniform bounded wait: every lane gets the same answer, so warp-collective instructions

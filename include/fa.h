@@ -171,6 +171,17 @@ fa_status_t fa_decode_splitkv_noalloc(const fa_bf16_t* q, const fa_bf16_t* k, co
  */
 fa_status_t fa_sync_status(void* stream);
 
+/*
+ * fa_selftest_wait_timeout -- diagnostic for the library's failure detection.  Enqueues one
+ * tiny kernel that waits, with the bounded wait every pipeline here uses, on an mbarrier that
+ * nothing ever arrives at; after ``limit_us`` microseconds it records a timeout and returns.
+ * The following fa_sync_status(stream) then reports FA_ERR_DEVICE_TIMEOUT (and clears it), and
+ * the CUDA context stays usable.  Failing loudly instead of hanging or silently producing
+ * garbage is the behaviour [Scratch] "How this shows up in practice" asks for.  limit_us must
+ * be in [1, 10^7]; otherwise FA_ERR_INVALID_ARG.
+ */
+fa_status_t fa_selftest_wait_timeout(unsigned int limit_us, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* fa_status_string(fa_status_t status);
 

@@ -116,3 +116,8 @@ def test_library_source_never_allocates():
     for fn in os.listdir(CSRC):
         text = open(os.path.join(CSRC, fn)).read()
         assert "cudaMalloc" not in text and "cudaFree" not in text, fn
+
+
+def test_selftest_rejects_bad_limits(lib):
+    assert lib.fa_selftest_wait_timeout(0, None) == INVALID
+    assert lib.fa_selftest_wait_timeout(20 * 1000 * 1000, None) == INVALID
