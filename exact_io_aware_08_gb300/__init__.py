@@ -18,7 +18,7 @@ __all__ = [
     "FaError", "load_library", "library_path",
     "fa_fwd", "fa_bwd", "fa_bwd_prep", "fa_bwd_main", "fa_bwd_finish", "fa_decode_splitkv", "fa_bwd_workspace_size", "fa_decode_splitkv_noalloc",
     "fa_decode_workspace_size", "fa_sync_status", "fa_status_string", "fa_last_error_message",
-    "forward", "backward", "decode",
+    "forward", "backward", "decode", "fa_fwd_varlen", "forward_varlen",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -48,6 +48,7 @@ _S = ctypes.c_size_t
 
 _SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_workspace_size": (_S, [_I, _I, _I, _I, _I]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_prep": (_I, [_P, _P, _P, _S, _I, _I, _I, _I, _I, _P]),
@@ -113,6 +114,31 @@ def fa_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None):
     B, H, n_q, n_kv, d = _dims(q, k)
     _check(load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, n_q, n_kv,
                                  d, float(scale), int(bool(causal)), _stream(stream)))
+
+
+def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                  max_seqlen_k: int, scale: float, causal: bool, stream=None):
+    """Packed variable-length forward: q/o [total_q, H, d], k/v [total_k, H, d], lse [H, total_q],
+    cu_seqlens_* int32 device tensors of n_seqs + 1 boundaries."""
+    total_q, H, d = q.shape
+    total_k = k.shape[0]
+    n_seqs = cu_seqlens_q.numel() - 1
+    _check(load_library().fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                        _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), n_seqs, H, total_q,
+                                        total_k, int(max_seqlen_q), int(max_seqlen_k), d,
+                                        float(scale), int(bool(causal)), _stream(stream)))
+
+
+def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                   causal: bool = False, scale: float | None = None, stream=None):
+    """Returns (O [total_q, H, d] bf16, lse [H, total_q] fp32)."""
+    import torch
+    scale = q.shape[-1] ** -0.5 if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device)
+    fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, scale,
+                  causal, stream)
+    return o, lse
 
 
 def fa_bwd_workspace_size(B: int, H: int, n_q: int, n_kv: int, d: int) -> int:

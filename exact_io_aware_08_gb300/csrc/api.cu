@@ -83,6 +83,39 @@ fa_status_t fa_fwd(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v, f
   return FA_OK;
 }
 
+fa_status_t fa_fwd_varlen(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
+                          fa_bf16_t* o, float* lse, const int* cu_seqlens_q,
+                          const int* cu_seqlens_k, int n_seqs, int H, int total_q, int total_k,
+                          int max_seqlen_q, int max_seqlen_k, int d, float scale, int causal,
+                          void* stream) {
+  if (n_seqs < 1) return fail(FA_ERR_INVALID_ARG, "n_seqs must be >= 1 (got %d)", n_seqs);
+  if (total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
+    return fail(FA_ERR_INVALID_ARG, "totals and max sequence lengths must be >= 0");
+  if (max_seqlen_q > total_q || max_seqlen_k > total_k)
+    return fail(FA_ERR_INVALID_ARG, "max_seqlen exceeds the total token count");
+  fa_status_t st = check_shape(1, H, max_seqlen_q, max_seqlen_k, d, scale);
+  if (st != FA_OK) return st;
+  const long long lim = (1LL << 31) / (static_cast<long long>(d) * H);
+  if (total_q >= lim || total_k >= lim)
+    return fail(FA_ERR_UNSUPPORTED, "total tokens too large for H=%d d=%d", H, d);
+  const long long items = ((static_cast<long long>(max_seqlen_q) + 255) / 256) * n_seqs * H;
+  if (items >= (1LL << 31)) return fail(FA_ERR_UNSUPPORTED, "too many (block, sequence, head) items");
+  if (total_q == 0 || max_seqlen_q == 0) return FA_OK;
+  if (!q || !o || !lse || !cu_seqlens_q || !cu_seqlens_k || (total_k > 0 && (!k || !v)))
+    return fail(FA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(FA_ERR_INVALID_ARG, "arrays must be 16-byte aligned");
+  fa::FwdVarlenArgs a{};
+  a.q = q; a.k = total_k ? k : q; a.v = total_k ? v : q; a.o = o; a.lse = lse;
+  a.cu_q = cu_seqlens_q; a.cu_k = cu_seqlens_k;
+  a.n_seqs = n_seqs; a.H = H; a.total_q = total_q; a.total_k = total_k;
+  a.max_seqlen_q = max_seqlen_q; a.max_seqlen_k = max_seqlen_k; a.d = d; a.scale = scale;
+  a.causal = causal ? 1 : 0;
+  cudaError_t e = fa::launch_fwd_varlen(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_varlen launch");
+  return FA_OK;
+}
+
 size_t fa_bwd_workspace_size(int B, int H, int N_q, int N_kv, int d) {
   if (B < 1 || H < 1 || N_q < 0 || N_kv < 0 || (d != 64 && d != 128)) return 0;
   return fa::bwd_dq_acc_bytes(B, H, N_q, d) + fa::bwd_delta_bytes(B, H, N_q);
@@ -270,6 +303,10 @@ fa_status_t fa_sync_status(void* stream) {
   }
   if (code & fa::FA_DEV_TIMEOUT)
     return fail(FA_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait ran out (site %d)", where);
+  if (code & fa::FA_DEV_BAD_CONFIG)
+    return fail(FA_ERR_INVALID_ARG,
+                "a kernel found invalid sequence boundaries (cu_seqlens / max_seqlen) (site %d)",
+                where);
   if (code) return fail(FA_ERR_CUDA, "device reported error code %u (site %d)", code, where);
   return FA_OK;
 }

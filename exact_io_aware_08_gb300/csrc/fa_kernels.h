@@ -27,6 +27,19 @@ struct FwdArgs {
   int causal;
 };
 
+struct FwdVarlenArgs {
+  const void* q;     // [total_q, H, d]
+  const void* k;     // [total_k, H, d]
+  const void* v;
+  void* o;           // [total_q, H, d]
+  float* lse;        // [H, total_q]
+  const int* cu_q;   // [n_seqs + 1], device
+  const int* cu_k;
+  int n_seqs, H, total_q, total_k, max_seqlen_q, max_seqlen_k, d;
+  float scale;
+  int causal;
+};
+
 struct BwdArgs {
   const void* q;
   const void* k;
@@ -58,6 +71,7 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_fwd_varlen(const FwdVarlenArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t stream);    // F2
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream);    // F3
 cudaError_t launch_bwd_finish(const BwdArgs& a, cudaStream_t stream);  // F4

@@ -67,9 +67,15 @@ struct FwdParams {
   float* lse;
   int n_q, n_kv, n_qpairs, n_kvtiles, causal;
   float scale, scale_log2;
+  // Variable-length batches: packed token-major [total, H, d] tensors, sequence s occupying
+  // rows [cu_q[s], cu_q[s+1]) (queries) and [cu_k[s], cu_k[s+1]) (keys); lse is [H, total_q].
+  int heads, total_q;
+  const int* cu_q;
+  const int* cu_k;
+  uint16_t* o;                                        // for row-wise stores of a partial tile
 };
 
-template <int D>
+template <int D, bool VL>
 __global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
 fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
@@ -95,17 +101,41 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
 
   // Work item: query rows [256 c, 256 c + 256) of head bh.  Items of one head are adjacent so
   // the CTAs that run together share K/V in L2; causal runs each head's longer items first.
-  const int bh = blockIdx.x / p.n_qpairs;
+  // Variable-length: item = (sequence, head, 256-row block), sized by the longest sequence;
+  // blocks past a sequence's end exit at once.  Rows are then local to the sequence.
+  const int bh = blockIdx.x / p.n_qpairs;             // fixed length: (b, h) plane
   const int r = blockIdx.x % p.n_qpairs;
-  const int c = p.causal ? (p.n_qpairs - 1 - r) : r;
+  int n_q = p.n_q, n_kv = p.n_kv, q_beg = 0, k_beg = 0, head = 0;
+  if (VL) {
+    const int seq = bh / p.heads;
+    head = bh % p.heads;
+    q_beg = p.cu_q[seq];
+    n_q = p.cu_q[seq + 1] - q_beg;
+    k_beg = p.cu_k[seq];
+    n_kv = p.cu_k[seq + 1] - k_beg;
+    // Boundaries come from the caller's device arrays: check them here, so bad ones become a
+    // reported error instead of out-of-range rows (p.n_q = max_seqlen_q, p.n_kv = total_k).
+    if (q_beg < 0 || n_q < 0 || q_beg + n_q > p.total_q || n_q > p.n_q || k_beg < 0 || n_kv < 0 ||
+        k_beg + n_kv > p.n_kv) {
+      if (threadIdx.x == 0 && r == 0) report_device_error(FA_DEV_BAD_CONFIG, 150);
+      return;
+    }
+  }
+  const int n_qpairs = (n_q + 2 * C::BM - 1) / (2 * C::BM);
+  if (r >= n_qpairs) return;                          // whole CTA, before any shared state
+  const int n_kvtiles = (n_kv + C::BN - 1) / C::BN;
+  const int c = p.causal ? (n_qpairs - 1 - r) : r;
   int q0[2], n_t[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     q0[t] = c * 2 * C::BM + t * C::BM;
     const int tile_index = 2 * c + t;                 // in units of 128 rows
-    n_t[t] = (q0[t] >= p.n_q) ? 0 : (p.causal ? min(tile_index + 1, p.n_kvtiles) : p.n_kvtiles);
+    n_t[t] = (q0[t] >= n_q) ? 0 : (p.causal ? min(tile_index + 1, n_kvtiles) : n_kvtiles);
   }
   const int n_max = max(n_t[0], n_t[1]);
+  // TMA coordinates of local row ``row``: fixed length {x, row, (b,h)}; packed {x, h, beg+row}
+  auto y1 = [&](int row) { return VL ? head : row; };
+  auto y2 = [&](int beg, int row) { return VL ? beg + row : bh; };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -143,18 +173,18 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       mbar_arrive_expect_tx(q_full, nq_tiles * C::TILE);
       for (int t = 0; t < nq_tiles; ++t)
         for (int k = 0; k < C::KCH; ++k)
-          tma_load_3d(sQ + t * C::TILE + k * C::CHUNK, &p.tq, q_full, k * 64, q0[t], bh);
+          tma_load_3d(sQ + t * C::TILE + k * C::CHUNK, &p.tq, q_full, k * 64, y1(q0[t]), y2(q_beg, q0[t]));
       for (int j = 0; j < n_max; ++j) {
         const int s = j % C::NS;
         const uint32_t u = j / C::NS;
         if (u > 0 && !mbar_wait(&k_empty[s], (u - 1) & 1, abort_flag, 101)) break;
         mbar_arrive_expect_tx(&k_full[s], C::TILE);
         for (int k = 0; k < C::KCH; ++k)
-          tma_load_3d(sK + s * C::TILE + k * C::CHUNK, &p.tk, &k_full[s], k * 64, j * C::BN, bh);
+          tma_load_3d(sK + s * C::TILE + k * C::CHUNK, &p.tk, &k_full[s], k * 64, y1(j * C::BN), y2(k_beg, j * C::BN));
         if (u > 0 && !mbar_wait(&v_empty[s], (u - 1) & 1, abort_flag, 102)) break;
         mbar_arrive_expect_tx(&v_full[s], C::TILE);
         for (int k = 0; k < C::KCH; ++k)
-          tma_load_3d(sV + s * C::TILE + k * C::CHUNK, &p.tv, &v_full[s], k * 64, j * C::BN, bh);
+          tma_load_3d(sV + s * C::TILE + k * C::CHUNK, &p.tv, &v_full[s], k * 64, y1(j * C::BN), y2(k_beg, j * C::BN));
         issued = j + 1;
       }
       if (*abort_flag) {
@@ -262,8 +292,8 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       tmem_wait_ld();
 
       const int k0 = j * C::BN;
-      if (k0 + C::BN > p.n_kv || (p.causal && k0 + C::BN - 1 > q0[t])) {
-        const int lim = p.causal ? min(q_idx + 1, p.n_kv) : p.n_kv;   // keys < lim visible
+      if (k0 + C::BN > n_kv || (p.causal && k0 + C::BN - 1 > q0[t])) {
+        const int lim = p.causal ? min(q_idx + 1, n_kv) : n_kv;   // keys < lim visible
 #pragma unroll
         for (int k = 0; k < 128; ++k)
           if (k0 + k >= lim) s[k] = -INFINITY;
@@ -342,7 +372,11 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       tc_fence_after();
     }
     uint8_t* stage = sQ + t * C::TILE;         // Q_t is dead once o_done[t] fired
-    if (ok && q0[t] < p.n_q) {
+    // A packed tile that ends past its sequence is stored row by row (a TMA store of the
+    // whole box would write into the next sequence's rows).
+    const bool rowwise = VL && (q0[t] + C::BM > n_q);
+    uint16_t* orow = rowwise ? p.o + (static_cast<size_t>(q_beg + q_idx) * p.heads + head) * D : nullptr;
+    if (ok && q0[t] < n_q) {
       const float inv_l = (lb > 0.f) ? 1.f / lb : 0.f;
 #pragma unroll
       for (int k = 0; k < D / 32; ++k) {
@@ -362,17 +396,24 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
           v4.z = pack_bf16x2(__uint_as_float(rr[i + 4]) * inv_l, __uint_as_float(rr[i + 5]) * inv_l);
           v4.w = pack_bf16x2(__uint_as_float(rr[i + 6]) * inv_l, __uint_as_float(rr[i + 7]) * inv_l);
           const int col = k * 32 + i;
-          *reinterpret_cast<uint4*>(stage + (col >> 6) * C::CHUNK + sw128_offset(row, col & 63)) = v4;
+          if (rowwise) {
+            if (q_idx < n_q) *reinterpret_cast<uint4*>(orow + col) = v4;
+          } else {
+            *reinterpret_cast<uint4*>(stage + (col >> 6) * C::CHUNK + sw128_offset(row, col & 63)) = v4;
+          }
         }
       }
-      if (q_idx < p.n_q)
-        p.lse[static_cast<size_t>(bh) * p.n_q + q_idx] =
-            (l > 0.f) ? fmaf(m, p.scale, logf(l)) : -INFINITY;
+      if (q_idx < n_q) {
+        const size_t li = VL ? static_cast<size_t>(head) * p.total_q + q_beg + q_idx
+                                   : static_cast<size_t>(bh) * n_q + q_idx;
+        p.lse[li] = (l > 0.f) ? fmaf(m, p.scale, logf(l)) : -INFINITY;
+      }
       fence_proxy_async_smem();
     }
     named_bar_sync(1 + t, 128);
-    if (ok && q0[t] < p.n_q && (threadIdx.x & 127) == 64) {
-      for (int k = 0; k < C::KCH; ++k) tma_store_3d(&p.to, stage + k * C::CHUNK, k * 64, q0[t], bh);
+    if (ok && !rowwise && q0[t] < n_q && (threadIdx.x & 127) == 64) {
+      for (int k = 0; k < C::KCH; ++k)
+        tma_store_3d(&p.to, stage + k * C::CHUNK, k * 64, y1(q0[t]), y2(q_beg, q0[t]));
       bulk_commit_group();
       bulk_wait_group_read0();
     }
@@ -409,12 +450,56 @@ static cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   p.causal = a.causal;
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.heads = a.H;
+  p.total_q = 0;
+  p.cu_q = p.cu_k = nullptr;
+  p.o = static_cast<uint16_t*>(a.o);
   static int attr_done[64] = {0};   // one per instantiation of this launcher
-  cudaError_t e = ensure_smem_attr(fwd_kernel<D>, C::SMEM_BYTES, attr_done);
+  cudaError_t e = ensure_smem_attr(fwd_kernel<D, false>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
   const uint64_t grid = static_cast<uint64_t>(p.n_qpairs) * bh;
-  fwd_kernel<D><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
+  fwd_kernel<D, false><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
+}
+
+// Variable-length forward: packed token-major [total, H, d] tensors and cu_seqlens.
+template <int D>
+static cudaError_t launch_fwd_varlen_d(const FwdVarlenArgs& a, cudaStream_t stream) {
+  using C = FwdCfg<D>;
+  FwdParams p;
+  // {d, H, total}: a {64, 1, 128} box is 128 consecutive tokens of one head
+  auto make = [&](CUtensorMap* m, const void* base, int total) {
+    const int rows = total > 0 ? total : 1;
+    return make_map_bf16_tok(m, base, D, a.H, rows, 64, 128);
+  };
+  if (!make(&p.tq, a.q, a.total_q) || !make(&p.tk, a.k, a.total_k) || !make(&p.tv, a.v, a.total_k) ||
+      !make(&p.to, a.o, a.total_q))
+    return cudaErrorInvalidValue;
+  p.lse = a.lse;
+  p.n_q = a.max_seqlen_q;          // bound checked against every sequence in the kernel
+  p.n_kv = a.total_k;
+  p.n_qpairs = (a.max_seqlen_q + 2 * C::BM - 1) / (2 * C::BM);
+  p.n_kvtiles = 0;
+  p.causal = a.causal;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.heads = a.H;
+  p.total_q = a.total_q;
+  p.cu_q = a.cu_q;
+  p.cu_k = a.cu_k;
+  p.o = static_cast<uint16_t*>(a.o);
+  static int attr_done[64] = {0};
+  cudaError_t e = ensure_smem_attr(fwd_kernel<D, true>, C::SMEM_BYTES, attr_done);
+  if (e != cudaSuccess) return e;
+  const uint64_t grid = static_cast<uint64_t>(p.n_qpairs) * a.n_seqs * a.H;
+  if (grid == 0) return cudaSuccess;
+  fwd_kernel<D, true><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_varlen(const FwdVarlenArgs& a, cudaStream_t stream) {
+  if (a.d == 64) return launch_fwd_varlen_d<64>(a, stream);
+  return launch_fwd_varlen_d<128>(a, stream);
 }
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {

@@ -64,6 +64,31 @@ fa_status_t fa_fwd(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v, f
                    void* stream);
 
 /*
+ * fa_fwd_varlen -- attention forward over a batch of sequences of different lengths, packed
+ * without padding (variable-length batches with cu_seqlens boundaries, as [Scratch] "How this
+ * shows up in practice" describes; padding every sequence to the longest would pay for the
+ * padded work).  Same computation as fa_fwd, per sequence.
+ *
+ *  q, o : [total_q, H, d] bf16, token-major (token t of all heads, then token t+1, ...)
+ *  k, v : [total_k, H, d] bf16
+ *  lse  : [H, total_q] fp32, natural log
+ *  cu_seqlens_q, cu_seqlens_k : DEVICE int arrays of n_seqs + 1 entries; sequence s owns query
+ *         rows [cu_q[s], cu_q[s+1]) and key rows [cu_k[s], cu_k[s+1]); non-decreasing, starting
+ *         at 0 and ending at total_q / total_k.
+ *  max_seqlen_q, max_seqlen_k : upper bounds on the per-sequence lengths (size the launch).
+ *  causal : query i of a sequence sees that sequence's keys j <= i (positions within the
+ *         sequence; meant for self-attention, where each sequence's two lengths are equal).
+ * The kernels check every boundary they read; a boundary outside [0, total] or a length above
+ * max_seqlen_q makes the affected work item write nothing and fa_sync_status report
+ * FA_ERR_INVALID_ARG.  A sequence with no keys gets O = 0 and lse = -inf.
+ */
+fa_status_t fa_fwd_varlen(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
+                          fa_bf16_t* o, float* lse, const int* cu_seqlens_q,
+                          const int* cu_seqlens_k, int n_seqs, int H, int total_q, int total_k,
+                          int max_seqlen_q, int max_seqlen_k, int d, float scale, int causal,
+                          void* stream);
+
+/*
  * Workspace bytes fa_bwd needs: an fp32 dQ accumulator [B,H,N_q,d] plus fp32 D [B,H,N_q]
  * plus alignment padding.  Returns 0 for unsupported arguments.
  */
