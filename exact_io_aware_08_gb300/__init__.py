@@ -19,6 +19,7 @@ __all__ = [
     "fa_fwd", "fa_bwd", "fa_bwd_prep", "fa_bwd_main", "fa_bwd_finish", "fa_decode_splitkv", "fa_bwd_workspace_size", "fa_decode_splitkv_noalloc",
     "fa_decode_workspace_size", "fa_sync_status", "fa_status_string", "fa_last_error_message",
     "forward", "backward", "decode", "fa_fwd_varlen", "forward_varlen",
+    "fa_bwd_varlen", "backward_varlen",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -50,6 +51,8 @@ _SIGNATURES = {
     "fa_fwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_workspace_size": (_S, [_I, _I, _I, _I, _I]),
+    "fa_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _P, _P, _I, _I, _I, _I, _I, _I,
+                           _I, _F, _I, _P]),
     "fa_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _I, _F, _I, _P]),
     "fa_bwd_prep": (_I, [_P, _P, _P, _S, _I, _I, _I, _I, _I, _P]),
     "fa_bwd_main": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _I, _F, _I, _P]),
@@ -139,6 +142,31 @@ def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen
     fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, scale,
                   causal, stream)
     return o, lse
+
+
+def fa_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, ws, cu_seqlens_q, cu_seqlens_k,
+                  max_seqlen_q: int, max_seqlen_k: int, scale: float, causal: bool, stream=None):
+    total_q, H, d = q.shape
+    _check(load_library().fa_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), _nbytes(ws),
+                                        _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+                                        cu_seqlens_q.numel() - 1, H, total_q, k.shape[0],
+                                        int(max_seqlen_q), int(max_seqlen_k), d, float(scale),
+                                        int(bool(causal)), _stream(stream)))
+
+
+def backward_varlen(q, k, v, o, lse, do, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                    causal: bool = False, scale: float | None = None, stream=None):
+    """Returns (dQ, dK, dV) for packed [total, H, d] tensors."""
+    import torch
+    total_q, H, d = q.shape
+    scale = d ** -0.5 if scale is None else scale
+    ws = torch.empty(max(fa_bwd_workspace_size(1, H, total_q, k.shape[0], d), 256), dtype=torch.uint8,
+                     device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_bwd_varlen(q, k, v, o, lse, do, dq, dk, dv, ws, cu_seqlens_q, cu_seqlens_k, max_seqlen_q,
+                  max_seqlen_k, scale, causal, stream)
+    return dq, dk, dv
 
 
 def fa_bwd_workspace_size(B: int, H: int, n_q: int, n_kv: int, d: int) -> int:

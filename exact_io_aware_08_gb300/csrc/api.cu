@@ -215,6 +215,45 @@ fa_status_t fa_bwd_finish(fa_bf16_t* dq, const void* ws, size_t ws_bytes, int B,
   return e == cudaSuccess ? FA_OK : cuda_fail(e, "fa_bwd_finish launch");
 }
 
+fa_status_t fa_bwd_varlen(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
+                          const fa_bf16_t* o, const float* lse, const fa_bf16_t* dO,
+                          fa_bf16_t* dq, fa_bf16_t* dk, fa_bf16_t* dv, void* ws, size_t ws_bytes,
+                          const int* cu_seqlens_q, const int* cu_seqlens_k, int n_seqs, int H,
+                          int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
+                          float scale, int causal, void* stream) {
+  if (n_seqs < 1) return fail(FA_ERR_INVALID_ARG, "n_seqs must be >= 1 (got %d)", n_seqs);
+  if (total_q < 0 || total_k < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
+    return fail(FA_ERR_INVALID_ARG, "totals and max sequence lengths must be >= 0");
+  if (max_seqlen_q > total_q || max_seqlen_k > total_k)
+    return fail(FA_ERR_INVALID_ARG, "max_seqlen exceeds the total token count");
+  if (!cu_seqlens_q || !cu_seqlens_k) return fail(FA_ERR_INVALID_ARG, "null cu_seqlens");
+  const long long lim = (1LL << 31) / (static_cast<long long>(d > 0 ? d : 1) * (H > 0 ? H : 1));
+  if (total_q >= lim || total_k >= lim)
+    return fail(FA_ERR_UNSUPPORTED, "total tokens too large for H=%d d=%d", H, d);
+  const long long items = ((static_cast<long long>(max_seqlen_k) + 127) / 128) * n_seqs * (H > 0 ? H : 1);
+  if (items >= (1LL << 31)) return fail(FA_ERR_UNSUPPORTED, "too many (key tile, sequence, head) items");
+  // the packed layout is one [1, H, total, d]-sized problem for the prep and finish steps
+  fa::BwdArgs a;
+  const void* const ptrs[9] = {q, k, v, o, lse, dO, dq, dk, dv};
+  fa_status_t st = check_bwd(ptrs, kNeedAll, ws, ws_bytes, 1, H, total_q, total_k, d, scale, 0, &a);
+  if (st != FA_OK) return st;
+  if (total_q == 0 && total_k == 0) return FA_OK;
+  a.causal = causal ? 1 : 0;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = cu_seqlens_k;
+  a.n_seqs = n_seqs;
+  a.total_q = total_q;
+  a.total_k = total_k;
+  a.max_seqlen_q = max_seqlen_q;
+  a.max_seqlen_k = max_seqlen_k;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = fa::launch_bwd_prep(a, s);
+  if (e == cudaSuccess) e = fa::launch_bwd_main(a, s);
+  if (e == cudaSuccess) e = fa::launch_bwd_finish(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_bwd_varlen launch");
+  return FA_OK;
+}
+
 size_t fa_decode_workspace_size(int B, int H, int N_kv, int d, int n_splits) {
   if (B < 1 || H < 1 || N_kv < 0 || (d != 64 && d != 128)) return 0;
   if (n_splits <= 0) n_splits = fa::decode_auto_splits(B, H, N_kv);

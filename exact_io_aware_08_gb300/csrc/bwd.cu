@@ -77,6 +77,13 @@ struct BwdParams {
   float* dq_acc;
   int n_q, n_kv, n_qtiles, n_kvtiles, causal;
   float scale, scale_log2;
+  // Variable-length batches (packed token-major [total, H, d]; lse [H, total_q]; D and the dQ
+  // accumulator in the packed row order (token * H + head)).
+  int heads, total_q, total_k, max_q, max_k;
+  const int* cu_q;
+  const int* cu_k;
+  uint16_t* dk;
+  uint16_t* dv;
 };
 
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
@@ -88,7 +95,7 @@ __device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float
                :: "l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
-template <int D>
+template <int D, bool VL>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 bwd_main_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
@@ -114,11 +121,35 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
   const int lane = threadIdx.x & 31;
 
   // Work item: key tile kt of head bh; causal key tiles with more query tiles run first.
-  const int bh = blockIdx.x / p.n_kvtiles;
+  const int bh = blockIdx.x / p.n_kvtiles;           // fixed length: (b, h) plane
   const int kt = blockIdx.x % p.n_kvtiles;
   const int k0 = kt * C::BN;
+  int n_q = p.n_q, n_kv = p.n_kv, q_beg = 0, k_beg = 0, head = 0;
+  if (VL) {
+    // item = (sequence, head, key tile) sized by the longest sequence; boundaries are checked
+    const int seq = bh / p.heads;
+    head = bh % p.heads;
+    q_beg = p.cu_q[seq];
+    n_q = p.cu_q[seq + 1] - q_beg;
+    k_beg = p.cu_k[seq];
+    n_kv = p.cu_k[seq + 1] - k_beg;
+    if (q_beg < 0 || n_q < 0 || q_beg + n_q > p.total_q || n_q > p.max_q || k_beg < 0 ||
+        n_kv < 0 || k_beg + n_kv > p.total_k || n_kv > p.max_k) {
+      if (threadIdx.x == 0 && kt == 0) report_device_error(FA_DEV_BAD_CONFIG, 250);
+      return;
+    }
+    if (k0 >= n_kv) return;                         // whole CTA, before any shared state
+  }
+  const int n_qtiles = (n_q + C::BM - 1) / C::BM;
   const int i_start = p.causal ? (k0 / C::BM) : 0;     // first query tile that sees key k0
-  const int n = max(0, p.n_qtiles - i_start);
+  const int n = max(0, n_qtiles - i_start);
+  // TMA coordinates of local row ``row``: fixed length {x, row, (b,h)}; packed {x, h, beg+row}
+  auto y1 = [&](int row) { return VL ? head : row; };
+  auto y2 = [&](int beg, int row) { return VL ? beg + row : bh; };
+  // packed-row index of local query q: fixed [B*H, N] order, packed token * H + head
+  auto qrow = [&](int q) -> size_t {
+    return VL ? static_cast<size_t>(q_beg + q) * p.heads + head : static_cast<size_t>(bh) * n_q + q;
+  };
 
   auto stage_ptr = [&](int s) { return smem + C::OFF_ST + s * C::STAGE; };
 
@@ -156,8 +187,8 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       if (lane == 0) {
         mbar_arrive_expect_tx(kv_full, 2 * C::KV_TILE);
         for (int c = 0; c < C::KCH; ++c) {
-          tma_load_3d(sK + c * C::KV_CHUNK, &p.tk, kv_full, c * 64, k0, bh);
-          tma_load_3d(sV + c * C::KV_CHUNK, &p.tv, kv_full, c * 64, k0, bh);
+          tma_load_3d(sK + c * C::KV_CHUNK, &p.tk, kv_full, c * 64, y1(k0), y2(k_beg, k0));
+          tma_load_3d(sV + c * C::KV_CHUNK, &p.tv, kv_full, c * 64, y1(k0), y2(k_beg, k0));
         }
       }
       int issued = 0;
@@ -171,17 +202,18 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
         if (lane == 0) {
           mbar_arrive_expect_tx(&stage_full[s], 2 * C::Q_TILE);
           for (int c = 0; c < C::KCH; ++c) {
-            tma_load_3d(st + c * C::Q_CHUNK, &p.tq, &stage_full[s], c * 64, q0, bh);
-            tma_load_3d(st + C::Q_TILE + c * C::Q_CHUNK, &p.tdo, &stage_full[s], c * 64, q0, bh);
+            tma_load_3d(st + c * C::Q_CHUNK, &p.tq, &stage_full[s], c * 64, y1(q0), y2(q_beg, q0));
+            tma_load_3d(st + C::Q_TILE + c * C::Q_CHUNK, &p.tdo, &stage_full[s], c * 64, y1(q0),
+                        y2(q_beg, q0));
           }
         }
         float* s_lse = reinterpret_cast<float*>(st + 2 * C::Q_TILE);
         float* s_del = s_lse + C::BM;
-        const size_t rowbase = static_cast<size_t>(bh) * p.n_q;
         for (int e = lane; e < C::BM; e += 32) {
           const int q = q0 + e;
-          s_lse[e] = (q < p.n_q) ? -p.lse[rowbase + q] * 1.4426950408889634f : -INFINITY;
-          s_del[e] = (q < p.n_q) ? -p.delta[rowbase + q] : 0.f;
+          const size_t li = VL ? static_cast<size_t>(head) * p.total_q + q_beg + q : qrow(q);
+          s_lse[e] = (q < n_q) ? -p.lse[li] * 1.4426950408889634f : -INFINITY;
+          s_del[e] = (q < n_q) ? -p.delta[qrow(q)] : 0.f;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&stage_full[s]);
@@ -279,7 +311,7 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
     const int r = sub * 32 + lane;                 // key row within the tile
     const uint32_t t_lane = static_cast<uint32_t>(sub * 32) << 16;
     const int k_idx = k0 + r;
-    const bool row_dead = k_idx >= p.n_kv;
+    const bool row_dead = k_idx >= n_kv;
     const float c2 = p.scale_log2;
     bool ok = true;
     for (int i = 0; i < n; ++i) {
@@ -345,10 +377,16 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       ok = mbar_wait_warp(mma_done, 0, abort_flag, 223);
       tc_fence_after();
     }
+    // A packed key tile that ends past its sequence is stored row by row (a TMA store of the
+    // whole box would write into the next sequence's rows).
+    const bool rowwise = VL && (k0 + C::BN > n_kv);
     if (ok) {
       {
         const int which = grp;                        // group 0 writes dV, group 1 dK
         uint8_t* dst = which ? sK : sV;               // operands are dead once mma_done fired
+        uint16_t* grow = rowwise ? (which ? p.dk : p.dv) +
+                                       (static_cast<size_t>(k_beg + k_idx) * p.heads + head) * D
+                                 : nullptr;
         const uint32_t tcol = which ? C::T_DK : C::T_DV;
         const float mul = which ? p.scale : 1.f;
 #pragma unroll
@@ -369,17 +407,21 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
             v4.z = pack_bf16x2(__uint_as_float(rr[e + 4]) * mul, __uint_as_float(rr[e + 5]) * mul);
             v4.w = pack_bf16x2(__uint_as_float(rr[e + 6]) * mul, __uint_as_float(rr[e + 7]) * mul);
             const int col = c * 32 + e;
-            *reinterpret_cast<uint4*>(dst + (col >> 6) * C::KV_CHUNK + sw128_offset(r, col & 63)) = v4;
+            if (rowwise) {
+              if (!row_dead) *reinterpret_cast<uint4*>(grow + col) = v4;
+            } else {
+              *reinterpret_cast<uint4*>(dst + (col >> 6) * C::KV_CHUNK + sw128_offset(r, col & 63)) = v4;
+            }
           }
         }
       }
       fence_proxy_async_smem();
     }
     named_bar_sync(1, C::DS_THREADS);
-    if (ok && threadIdx.x == 64) {
+    if (ok && !rowwise && threadIdx.x == 64) {
       for (int c = 0; c < C::KCH; ++c) {
-        tma_store_3d(&p.tdk, sK + c * C::KV_CHUNK, c * 64, k0, bh);
-        tma_store_3d(&p.tdv, sV + c * C::KV_CHUNK, c * 64, k0, bh);
+        tma_store_3d(&p.tdk, sK + c * C::KV_CHUNK, c * 64, y1(k0), y2(k_beg, k0));
+        tma_store_3d(&p.tdv, sV + c * C::KV_CHUNK, c * 64, y1(k0), y2(k_beg, k0));
       }
       bulk_commit_group();
       bulk_wait_group_read0();
@@ -401,14 +443,15 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
         tmem_wait_ld();
         if constexpr (D == 128) {
           // lane = d, columns = queries q0 + c*32 + e
-          float* base = p.dq_acc + (static_cast<size_t>(bh) * p.n_q + q0 + c * 32) * D + rr_;
+          float* base = p.dq_acc + qrow(q0 + c * 32) * D + rr_;
+          const size_t step = VL ? static_cast<size_t>(p.heads) * D : static_cast<size_t>(D);
 #pragma unroll
           for (int e = 0; e < 32; ++e)
-            if (q0 + c * 32 + e < p.n_q) red_add_f32(base + static_cast<size_t>(e) * D, __uint_as_float(v[e]));
+            if (q0 + c * 32 + e < n_q) red_add_f32(base + e * step, __uint_as_float(v[e]));
         } else {
           // lane = query q0 + rr_, columns = d
-          if (q0 + rr_ < p.n_q) {
-            float* base = p.dq_acc + (static_cast<size_t>(bh) * p.n_q + q0 + rr_) * D + c * 32;
+          if (q0 + rr_ < n_q) {
+            float* base = p.dq_acc + qrow(q0 + rr_) * D + c * 32;
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
               red_add_v4_f32(base + e, __uint_as_float(v[e]), __uint_as_float(v[e + 1]),
@@ -517,11 +560,58 @@ static cudaError_t launch_bwd_main_d(const BwdArgs& a, cudaStream_t stream) {
   p.causal = a.causal;
   p.scale = a.scale;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.heads = a.H;
+  p.total_q = p.total_k = p.max_q = p.max_k = 0;
+  p.cu_q = p.cu_k = nullptr;
+  p.dk = static_cast<uint16_t*>(a.dk);
+  p.dv = static_cast<uint16_t*>(a.dv);
   static int attr_done[64] = {0};   // one per instantiation of this launcher
-  cudaError_t e = ensure_smem_attr(bwd_main_kernel<D>, C::SMEM_BYTES, attr_done);
+  cudaError_t e = ensure_smem_attr(bwd_main_kernel<D, false>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
   const uint64_t grid = static_cast<uint64_t>(p.n_kvtiles) * bh;
-  bwd_main_kernel<D><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
+  bwd_main_kernel<D, false><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// Variable-length main kernel: packed [total, H, d] tensors, cu_seqlens boundaries.
+template <int D>
+static cudaError_t launch_bwd_main_varlen_d(const BwdArgs& a, cudaStream_t stream) {
+  using C = BwdCfg<D>;
+  if (a.total_k == 0 || a.max_seqlen_k == 0) return cudaSuccess;
+  BwdParams p;
+  const int tq = a.total_q > 0 ? a.total_q : 1;
+  const void* qb = a.total_q > 0 ? a.q : a.k;
+  const void* dob = a.total_q > 0 ? a.dO : a.k;
+  if (!make_map_bf16_tok(&p.tq, qb, D, a.H, tq, 64, C::BM) ||
+      !make_map_bf16_tok(&p.tdo, dob, D, a.H, tq, 64, C::BM) ||
+      !make_map_bf16_tok(&p.tk, a.k, D, a.H, a.total_k, 64, C::BN) ||
+      !make_map_bf16_tok(&p.tv, a.v, D, a.H, a.total_k, 64, C::BN) ||
+      !make_map_bf16_tok(&p.tdk, a.dk, D, a.H, a.total_k, 64, C::BN) ||
+      !make_map_bf16_tok(&p.tdv, a.dv, D, a.H, a.total_k, 64, C::BN))
+    return cudaErrorInvalidValue;
+  p.lse = a.lse;
+  p.delta = a.delta;
+  p.dq_acc = a.dq_acc;
+  p.n_q = p.n_kv = 0;
+  p.n_qtiles = 0;
+  p.n_kvtiles = (a.max_seqlen_k + C::BN - 1) / C::BN;
+  p.causal = a.causal;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.heads = a.H;
+  p.total_q = a.total_q;
+  p.total_k = a.total_k;
+  p.max_q = a.max_seqlen_q;
+  p.max_k = a.max_seqlen_k;
+  p.cu_q = a.cu_q;
+  p.cu_k = a.cu_k;
+  p.dk = static_cast<uint16_t*>(a.dk);
+  p.dv = static_cast<uint16_t*>(a.dv);
+  static int attr_done[64] = {0};
+  cudaError_t e = ensure_smem_attr(bwd_main_kernel<D, true>, C::SMEM_BYTES, attr_done);
+  if (e != cudaSuccess) return e;
+  const uint64_t grid = static_cast<uint64_t>(p.n_kvtiles) * a.n_seqs * a.H;
+  bwd_main_kernel<D, true><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -540,6 +630,7 @@ cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t s) {
   return a.d == 64 ? launch_bwd_prep_d<64>(a, s) : launch_bwd_prep_d<128>(a, s);
 }
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t s) {
+  if (a.cu_q) return a.d == 64 ? launch_bwd_main_varlen_d<64>(a, s) : launch_bwd_main_varlen_d<128>(a, s);
   return a.d == 64 ? launch_bwd_main_d<64>(a, s) : launch_bwd_main_d<128>(a, s);
 }
 cudaError_t launch_bwd_finish(const BwdArgs& a, cudaStream_t s) {

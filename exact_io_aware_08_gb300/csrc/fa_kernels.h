@@ -55,6 +55,11 @@ struct BwdArgs {
   int B, H, n_q, n_kv, d;
   float scale;
   int causal;
+  // variable-length batches (cu_q != nullptr): packed [total, H, d] tensors; the prep and
+  // finish steps then run over B = 1, n_q = total_q rows of the packed layout
+  const int* cu_q = nullptr;
+  const int* cu_k = nullptr;
+  int n_seqs = 0, total_q = 0, total_k = 0, max_seqlen_q = 0, max_seqlen_k = 0;
 };
 
 struct DecodeArgs {

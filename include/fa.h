@@ -137,6 +137,21 @@ fa_status_t fa_bwd_finish(fa_bf16_t* dq, const void* ws, size_t ws_bytes, int B,
                           int N_kv, int d, float scale, void* stream);
 
 /*
+ * fa_bwd_varlen -- backward pass for fa_fwd_varlen: same computation as fa_bwd, per sequence,
+ * on packed token-major tensors (q, o, dO, dq: [total_q, H, d]; k, v, dk, dv: [total_k, H, d];
+ * lse: [H, total_q]) with the same device cu_seqlens arrays and bounds as the forward.  ``ws``
+ * holds at least fa_bwd_workspace_size(1, H, total_q, total_k, d) bytes, 256-byte aligned.
+ * Invalid boundaries are checked in the kernel and reported by fa_sync_status as for the
+ * forward.  dq is accumulated with fp32 atomics (last-bit run-to-run differences).
+ */
+fa_status_t fa_bwd_varlen(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
+                          const fa_bf16_t* o, const float* lse, const fa_bf16_t* dO,
+                          fa_bf16_t* dq, fa_bf16_t* dk, fa_bf16_t* dv, void* ws, size_t ws_bytes,
+                          const int* cu_seqlens_q, const int* cu_seqlens_k, int n_seqs, int H,
+                          int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
+                          float scale, int causal, void* stream);
+
+/*
  * Workspace bytes fa_decode_splitkv needs for n_splits partial states per (b, h):
  * fp32 (m, l, o~[d]).  n_splits <= 0 means "automatic" (as fa_decode_splitkv chooses).
  */
