@@ -10,6 +10,7 @@ Also measured in the same run and reported in the same JSON line:
   breakdown.fwd            forward alone, same workload
   breakdown.*_causal       the causal variant of the workload
   breakdown.decode         split-KV decode (B=64, H=32, N_kv=32768, d=128, 64 splits), GB/s
+  breakdown.decode_paged   the same decode over a paged cache (256-key blocks, shuffled), GB/s
   roofline                 the dominant kernel of the step (backward main kernel), timed alone
   e2e                      the step through the public Python API with host (pinned) buffers,
                            host->device and device->host copies inside the timed region
@@ -417,8 +418,42 @@ def run_ours(args, rank, world, local_rank):
                      "kernels": "decode_split_kernel<128> + decode_merge_kernel<128> (one call)",
                      "work_per_launch": f"{bytes_dec} B (K + V + q + O + lse)"},
     }
-    clocks = sampler.stop()
+
+    # ---- the same decode over a paged cache: 256-key blocks in a shuffled pool
+    bs = 256
+    nb = wd.N_kv // bs
+    perm = torch.randperm(wd.B * nb, generator=torch.Generator().manual_seed(wd.seed)).to(dev)
+
+    def paged(t):                                   # [B,H,N,d] -> [B*nb, bs, H, d] in pool order
+        blocks = t.view(wd.B, wd.H, nb, bs, wd.d).permute(0, 2, 3, 1, 4).reshape(wd.B * nb, bs, wd.H, wd.d)
+        pool = torch.empty_like(blocks)
+        pool[perm] = blocks
+        return pool
+    kc = paged(xd["k"])
+    vc = paged(xd["v"])
+    qd = xd["q"]
     del xd
+    torch.cuda.empty_cache()
+    table = perm.view(wd.B, nb).to(torch.int32).contiguous()
+    seqlens = torch.full((wd.B,), wd.N_kv, dtype=torch.int32, device=dev)
+
+    def dec_paged(pe):
+        if pe is not None:
+            pe[0].record(stream)
+        fa.fa_decode_paged(qd, kc, vc, od, lsed, table, seqlens, wd.N_kv, wd.scale, wd.n_splits, wsd)
+        if pe is not None:
+            pe[1].record(stream)
+    dp_total, dp_inner = timed(dec_paged, K, inner=True)
+    dp_ms = reduce_max(dp_total / K)
+    gbs_p = bytes_dec / (statistics.mean(dp_inner) * 1e-3) / 1e9
+    breakdown["decode_paged"] = {
+        "workload": f"{wd.name}, paged cache (block_size {bs}, blocks shuffled over the pool)",
+        "gbps": round(whole_job_rate(bytes_dec, world, dp_ms * 1e-3) / 1e9, 1),
+        "ms": round(dp_ms, 4), "frac_of_hbm": round(gbs_p / peak_hbm, 4),
+        "kernels": "decode_split_kernel<128, paged> + decode_merge_kernel<128> (one call)",
+    }
+    clocks = sampler.stop()
+    del qd, kc, vc
     torch.cuda.empty_cache()
 
     result = {

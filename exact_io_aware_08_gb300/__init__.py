@@ -19,7 +19,7 @@ __all__ = [
     "fa_fwd", "fa_bwd", "fa_bwd_prep", "fa_bwd_main", "fa_bwd_finish", "fa_decode_splitkv", "fa_bwd_workspace_size", "fa_decode_splitkv_noalloc",
     "fa_decode_workspace_size", "fa_sync_status", "fa_status_string", "fa_last_error_message",
     "forward", "backward", "decode", "fa_fwd_varlen", "forward_varlen",
-    "fa_bwd_varlen", "backward_varlen",
+    "fa_bwd_varlen", "backward_varlen", "fa_decode_paged", "decode_paged",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -60,6 +60,8 @@ _SIGNATURES = {
     "fa_decode_workspace_size": (_S, [_I, _I, _I, _I, _I]),
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
     "fa_decode_splitkv_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S,
+                             _P]),
     "fa_sync_status": (_I, [_P]),
     "fa_selftest_wait_timeout": (_I, [ctypes.c_uint, _P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
@@ -227,6 +229,20 @@ def fa_decode_splitkv_noalloc(q, k, v, o, lse, scale: float, n_splits: int, stre
                                                     _stream(stream)))
 
 
+def fa_decode_paged(q, k_cache, v_cache, o, lse, block_table, seqlens_k, max_seqlen_k: int,
+                    scale: float, n_splits: int, ws, stream=None):
+    """q [B,H,1,d]; k/v cache [num_blocks, block_size, H, d]; block_table [B, max_blocks] int32;
+    seqlens_k [B] int32 (both on the device)."""
+    B, H, _, d = q.shape
+    num_blocks, block_size = k_cache.shape[0], k_cache.shape[1]
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load_library().fa_decode_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse),
+                                          _ptr(block_table), _ptr(seqlens_k), B, H,
+                                          block_table.shape[1], block_size, num_blocks,
+                                          int(max_seqlen_k), d, float(scale), int(n_splits),
+                                          _ptr(ws), ws_bytes, _stream(stream)))
+
+
 def fa_sync_status(stream=None):
     _check(load_library().fa_sync_status(_stream(stream)))
 
@@ -286,4 +302,20 @@ def decode(q, k, v, n_splits: int = 0, scale: float | None = None, stream=None, 
     o = torch.empty_like(q)
     lse = torch.empty((B, H, 1), dtype=torch.float32, device=q.device)
     fa_decode_splitkv(q, k, v, o, lse, scale, n_splits, workspace, stream)
+    return o, lse
+
+
+def decode_paged(q, k_cache, v_cache, block_table, seqlens_k, max_seqlen_k: int, n_splits: int = 0,
+                 scale: float | None = None, stream=None, workspace=None):
+    """Split-KV decode over a paged cache -> (O [B,H,1,d], lse [B,H,1])."""
+    import torch
+    B, H, _, d = q.shape
+    scale = d ** -0.5 if scale is None else scale
+    need = fa_decode_workspace_size(B, H, max_seqlen_k, d, n_splits)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, 1), dtype=torch.float32, device=q.device)
+    fa_decode_paged(q, k_cache, v_cache, o, lse, block_table, seqlens_k, max_seqlen_k, scale,
+                    n_splits, workspace, stream)
     return o, lse

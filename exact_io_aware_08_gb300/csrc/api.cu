@@ -319,6 +319,52 @@ fa_status_t fa_decode_splitkv_noalloc(const fa_bf16_t* q, const fa_bf16_t* k, co
   return FA_OK;
 }
 
+fa_status_t fa_decode_paged(const fa_bf16_t* q, const fa_bf16_t* k_cache,
+                            const fa_bf16_t* v_cache, fa_bf16_t* o, float* lse,
+                            const int* block_table, const int* seqlens_k, int B, int H,
+                            int max_blocks_per_seq, int block_size, int num_blocks,
+                            int max_seqlen_k, int d, float scale, int n_splits, void* ws,
+                            size_t ws_bytes, void* stream) {
+  fa_status_t st = check_shape(B, H, 1, max_seqlen_k, d, scale);
+  if (st != FA_OK) return st;
+  if (block_size < 64 || block_size % 64 != 0)
+    return fail(FA_ERR_UNSUPPORTED, "block_size must be a positive multiple of 64 (got %d)",
+                block_size);
+  if (num_blocks < 1 || max_blocks_per_seq < 1)
+    return fail(FA_ERR_INVALID_ARG, "num_blocks and max_blocks_per_seq must be >= 1 (got %d, %d)",
+                num_blocks, max_blocks_per_seq);
+  if (static_cast<long long>(num_blocks) * block_size >= (1LL << 31))
+    return fail(FA_ERR_UNSUPPORTED, "num_blocks * block_size must be < 2^31");
+  if (static_cast<long long>(max_seqlen_k) > static_cast<long long>(max_blocks_per_seq) * block_size)
+    return fail(FA_ERR_INVALID_ARG, "max_seqlen_k=%d exceeds max_blocks_per_seq * block_size",
+                max_seqlen_k);
+  if (n_splits > fa::kDecodeMaxSplits)
+    return fail(FA_ERR_UNSUPPORTED, "n_splits=%d exceeds %d", n_splits, fa::kDecodeMaxSplits);
+  if (n_splits <= 0) n_splits = fa::decode_auto_splits(B, H, max_seqlen_k);
+  if (!q || !k_cache || !v_cache || !o || !lse || !block_table || !seqlens_k)
+    return fail(FA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+      !aligned16(lse))
+    return fail(FA_ERR_INVALID_ARG, "arrays must be 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(block_table) | reinterpret_cast<uintptr_t>(seqlens_k)) & 3u)
+    return fail(FA_ERR_INVALID_ARG, "block_table and seqlens_k must be 4-byte aligned");
+  const size_t need_ws = fa::decode_part_bytes(B, H, d, n_splits);
+  if (!ws || ws_bytes < need_ws || !aligned16(ws))
+    return fail(FA_ERR_WORKSPACE, "workspace must be >= %zu bytes and 16-byte aligned (got %zu)",
+                need_ws, ws_bytes);
+  fa::DecodePagedArgs a{};
+  a.q = q; a.k_cache = k_cache; a.v_cache = v_cache; a.o = o; a.lse = lse;
+  a.part = static_cast<float*>(ws);
+  a.block_table = block_table; a.seqlens = seqlens_k;
+  a.B = B; a.H = H; a.d = d; a.num_blocks = num_blocks; a.block_size = block_size;
+  a.max_blocks = max_blocks_per_seq; a.max_seqlen = max_seqlen_k;
+  a.scale = scale; a.n_splits = n_splits;
+  a.chunk = fa::decode_chunk(max_seqlen_k, n_splits);
+  cudaError_t e = fa::launch_decode_paged(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_decode_paged launch");
+  return FA_OK;
+}
+
 fa_status_t fa_selftest_wait_timeout(unsigned int limit_us, void* stream) {
   if (limit_us == 0 || limit_us > 10u * 1000u * 1000u)
     return fail(FA_ERR_INVALID_ARG, "limit_us must be in [1, 10000000] (got %u)", limit_us);

@@ -46,12 +46,17 @@ struct DecParams {
   float* part;
   int n_kv, bh, n_splits, chunk, n_items;
   float scale_log2;
+  // Paged KV cache: k/v cache [num_blocks, block_size, H, d]; logical key j of batch b lives in
+  // block block_table[b * max_blocks + j / block_size] at row j % block_size; seqlens[b] keys.
+  const int* block_table;
+  const int* seqlens;
+  int heads, block_size, max_blocks, num_blocks;
 };
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-template <int D>
+template <int D, bool PG>
 __global__ void __launch_bounds__(DecCfg<D>::THREADS, 2)
 decode_split_kernel(const __grid_constant__ DecParams p) {
   using C = DecCfg<D>;
@@ -78,10 +83,22 @@ decode_split_kernel(const __grid_constant__ DecParams p) {
   __syncthreads();
 
   // Sub-tiles of item i: keys [split*chunk, min(split*chunk + chunk, n_kv)) in steps of 64.
+  // Paged: the row's own length seqlens[b] (an out-of-range length is reported and treated as
+  // empty).
   auto item_subtiles = [&](int item, int& key0, int& key_end) {
     const int split = item % p.n_splits;
+    int n_kv = p.n_kv;
+    if (PG) {
+      // p.n_kv is the caller's max_seqlen_k (<= max_blocks * block_size, checked on the host),
+      // which the chunks cover
+      n_kv = p.seqlens[(item / p.n_splits) / p.heads];
+      if (n_kv < 0 || n_kv > p.n_kv) {
+        if (split == 0 && threadIdx.x == 0) report_device_error(FA_DEV_BAD_CONFIG, 350);
+        n_kv = 0;
+      }
+    }
     key0 = split * p.chunk;
-    key_end = min(key0 + p.chunk, p.n_kv);
+    key_end = min(key0 + p.chunk, n_kv);
     return key_end > key0 ? (key_end - key0 + C::KEYS - 1) / C::KEYS : 0;
   };
 
@@ -103,10 +120,23 @@ decode_split_kernel(const __grid_constant__ DecParams p) {
           uint8_t* st = smem + C::OFF_STAGE + s * C::STAGE;
           mbar_arrive_expect_tx(&full[s], C::STAGE);
           const int kk = key0 + t * C::KEYS;
+          int y1 = kk, y2 = bh;                     // contiguous cache: {x, key, (b,h)}
+          if (PG) {
+            // paged cache {x, h, block * block_size + row}; a 64-key sub-tile never crosses a
+            // block (block_size and the chunk are multiples of 64)
+            const int b = bh / p.heads;
+            int phys = p.block_table[static_cast<size_t>(b) * p.max_blocks + kk / p.block_size];
+            if (phys < 0 || phys >= p.num_blocks) {
+              report_device_error(FA_DEV_BAD_CONFIG, 351);
+              phys = 0;                             // stays in bounds; the result is reported invalid
+            }
+            y1 = bh % p.heads;
+            y2 = phys * p.block_size + kk % p.block_size;
+          }
 #pragma unroll
           for (int c = 0; c < C::KCH; ++c) {
-            tma_load_3d(st + c * C::CHUNK, &p.tk, &full[s], c * 64, kk, bh);
-            tma_load_3d(st + C::SUB + c * C::CHUNK, &p.tv, &full[s], c * 64, kk, bh);
+            tma_load_3d(st + c * C::CHUNK, &p.tk, &full[s], c * 64, y1, y2);
+            tma_load_3d(st + C::SUB + c * C::CHUNK, &p.tv, &full[s], c * 64, y1, y2);
           }
         }
       }
@@ -192,6 +222,9 @@ decode_split_kernel(const __grid_constant__ DecParams p) {
           for (int k = 0; k < 16; ++k) {
             const float pk = __shfl_sync(0xffffffffu, pv, k);
             const int r = warp * 16 + k;
+            // A paged block's rows past the sequence end are whatever the cache holds (possibly
+            // not finite): skip them rather than add 0 * V.
+            if (PG && key0 + t * C::KEYS + r >= key_end) break;
             const uint8_t* va = vb + r * 128 + ((unit ^ (r & 7)) << 4);
             if constexpr (C::VPL == 4) {
               const uint2 w = *reinterpret_cast<const uint2*>(va);
@@ -304,15 +337,59 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
   p.n_items = static_cast<int>(bh) * a.n_splits;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   static int attr_done[64] = {0};   // one per instantiation of this launcher
-  cudaError_t e = ensure_smem_attr(decode_split_kernel<D>, C::SMEM_BYTES, attr_done);
+  p.block_table = p.seqlens = nullptr;
+  p.heads = a.H;
+  p.block_size = p.max_blocks = p.num_blocks = 0;
+  cudaError_t e = ensure_smem_attr(decode_split_kernel<D, false>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
   const int grid = min(p.n_items, 2 * sm_count());
-  decode_split_kernel<D><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p);
+  decode_split_kernel<D, false><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   decode_merge_kernel<D><<<static_cast<unsigned>(bh), D, 0, stream>>>(
       a.part, static_cast<uint16_t*>(a.o), a.lse, a.n_splits);
   return cudaGetLastError();
+}
+
+// Paged KV cache decode: same split and merge kernels, cache rows found through the block table.
+template <int D>
+static cudaError_t launch_decode_paged_d(const DecodePagedArgs& a, cudaStream_t stream) {
+  using C = DecCfg<D>;
+  const uint64_t bh = static_cast<uint64_t>(a.B) * a.H;
+  DecParams p;
+  const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.block_size;
+  if (!make_map_bf16_tok(&p.tk, a.k_cache, D, a.H, rows, 64, C::KEYS) ||
+      !make_map_bf16_tok(&p.tv, a.v_cache, D, a.H, rows, 64, C::KEYS))
+    return cudaErrorInvalidValue;
+  p.q = static_cast<const uint16_t*>(a.q);
+  p.part = a.part;
+  p.n_kv = a.max_seqlen;
+  p.bh = static_cast<int>(bh);
+  p.n_splits = a.n_splits;
+  p.chunk = a.chunk;
+  p.n_items = static_cast<int>(bh) * a.n_splits;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.block_table = a.block_table;
+  p.seqlens = a.seqlens;
+  p.heads = a.H;
+  p.block_size = a.block_size;
+  p.max_blocks = a.max_blocks;
+  p.num_blocks = a.num_blocks;
+  static int attr_done[64] = {0};
+  cudaError_t e = ensure_smem_attr(decode_split_kernel<D, true>, C::SMEM_BYTES, attr_done);
+  if (e != cudaSuccess) return e;
+  const int grid = min(p.n_items, 2 * sm_count());
+  decode_split_kernel<D, true><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  decode_merge_kernel<D><<<static_cast<unsigned>(bh), D, 0, stream>>>(
+      a.part, static_cast<uint16_t*>(a.o), a.lse, a.n_splits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_paged(const DecodePagedArgs& a, cudaStream_t stream) {
+  if (a.d == 64) return launch_decode_paged_d<64>(a, stream);
+  return launch_decode_paged_d<128>(a, stream);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {

@@ -75,12 +75,27 @@ struct DecodeArgs {
   int chunk;         // keys per split (multiple of the kernel's key step)
 };
 
+struct DecodePagedArgs {
+  const void* q;            // [B, H, d]
+  const void* k_cache;      // [num_blocks, block_size, H, d]
+  const void* v_cache;
+  void* o;                  // [B, H, d]
+  float* lse;               // [B, H]
+  float* part;              // workspace, as for DecodeArgs
+  const int* block_table;   // [B, max_blocks], device
+  const int* seqlens;       // [B], device
+  int B, H, d, num_blocks, block_size, max_blocks, max_seqlen;
+  float scale;
+  int n_splits, chunk;
+};
+
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_fwd_varlen(const FwdVarlenArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t stream);    // F2
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream);    // F3
 cudaError_t launch_bwd_finish(const BwdArgs& a, cudaStream_t stream);  // F4
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_decode_paged(const DecodePagedArgs& a, cudaStream_t stream);
 
 // Per-TU device status accessors (see fa_status.cuh).
 cudaError_t status_fetch_fwd(cudaStream_t, unsigned int*, int*);

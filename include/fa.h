@@ -177,6 +177,36 @@ fa_status_t fa_decode_splitkv(const fa_bf16_t* q, const fa_bf16_t* k, const fa_b
                               void* stream);
 
 /*
+ * fa_decode_paged -- fa_decode_splitkv over a paged KV cache
+ * ([Lesson4] section 3 "Split-KV for decoding (flash-decoding)"; the cache paging itself is a
+ * serving-side layout the pages do not describe: the arithmetic is exactly that of
+ * fa_decode_splitkv on each row's first seqlens_k[b] keys).
+ *
+ * Layout: k_cache, v_cache [num_blocks, block_size, H, d] bf16 (token-major inside a block);
+ * block_table [B, max_blocks_per_seq] int32 on the device; seqlens_k [B] int32 on the device.
+ * Logical key j (0 <= j < seqlens_k[b]) of batch b lives in cache block
+ * block_table[b * max_blocks_per_seq + j / block_size] at row j % block_size.  Rows of a block
+ * past a sequence's end are never read into the result (they may hold anything).
+ * q: [B,H,1,d]; o: [B,H,1,d]; lse: [B,H,1].  A row with seqlens_k[b] == 0 gets O = 0 and
+ * lse = -inf.
+ *
+ *  - block_size must be a positive multiple of 64; num_blocks * block_size < 2^31;
+ *    max_seqlen_k <= max_blocks_per_seq * block_size (else FA_ERR_INVALID_ARG / UNSUPPORTED).
+ *  - The chunks of the split are sized from max_seqlen_k, which must bound every seqlens_k[b].
+ *  - Device-side checks: seqlens_k[b] outside [0, max_seqlen_k], or a block id outside
+ *    [0, num_blocks) in the part of the table a row uses, is recorded (the kernel stays in
+ *    bounds) and fa_sync_status then returns FA_ERR_INVALID_ARG; the outputs are undefined.
+ *  - ws: at least fa_decode_workspace_size(B, H, max_seqlen_k, d, n_splits) bytes, 16-byte
+ *    aligned.  n_splits as for fa_decode_splitkv.
+ */
+fa_status_t fa_decode_paged(const fa_bf16_t* q, const fa_bf16_t* k_cache,
+                            const fa_bf16_t* v_cache, fa_bf16_t* o, float* lse,
+                            const int* block_table, const int* seqlens_k, int B, int H,
+                            int max_blocks_per_seq, int block_size, int num_blocks,
+                            int max_seqlen_k, int d, float scale, int n_splits, void* ws,
+                            size_t ws_bytes, void* stream);
+
+/*
  * fa_decode_splitkv_noalloc -- fa_decode_splitkv for callers that cannot allocate device
  * memory (no counterpart in the pages; an interface convenience).
  *

@@ -121,3 +121,21 @@ def test_library_source_never_allocates():
 def test_selftest_rejects_bad_limits(lib):
     assert lib.fa_selftest_wait_timeout(0, None) == INVALID
     assert lib.fa_selftest_wait_timeout(20 * 1000 * 1000, None) == INVALID
+
+
+def test_paged_decode_rejection(lib):
+    """Host-side checks of fa_decode_paged: block size, table capacity, alignment, workspace."""
+    def call(block_size=128, num_blocks=8, max_blocks=4, max_seqlen=500, d=128, ws_bytes=1 << 30,
+             table=FAKE, seqlens=FAKE, n_splits=4):
+        return lib.fa_decode_paged(FAKE, FAKE, FAKE, FAKE, FAKE, table, seqlens, 2, 2, max_blocks,
+                                   block_size, num_blocks, max_seqlen, d, 0.1, n_splits, FAKE,
+                                   ws_bytes, None)
+    assert call(block_size=96) == UNSUPPORTED
+    assert call(block_size=32) == UNSUPPORTED
+    assert call(max_seqlen=513) == INVALID                    # 4 blocks of 128 hold 512 keys
+    assert call(num_blocks=0) == INVALID
+    assert call(table=None) == INVALID
+    assert call(seqlens=FAKE + 2) == INVALID
+    assert call(d=80) == UNSUPPORTED
+    assert call(ws_bytes=2 * 2 * 4 * 130 * 4 - 4) == WORKSPACE
+    assert call(num_blocks=1 << 24, block_size=256) == UNSUPPORTED   # rows past 2^31
