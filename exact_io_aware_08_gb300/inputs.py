@@ -91,3 +91,25 @@ def make_qkv(B: int, H: int, N_q: int, N_kv: int, d: int, seed: int, *,
 def make_workload(w: Workload, *, with_do: bool = True, device: str = "cpu"):
     return make_qkv(w.B, w.H, w.N_q, w.N_kv, w.d, w.seed, outlier_frac=w.outlier_frac,
                     with_do=with_do, device=device)
+
+
+FP8_E4M3_MAX = 448.0
+
+
+def make_qkv_fp8(B: int, H: int, N_q: int, N_kv: int, d: int, seed: int, *, device: str = "cpu"):
+    """FP8 inputs: the same fp32 ``randn`` draws as ``make_qkv`` (Q, K, V in that order), each
+    tensor given one scale s = amax / 448 and cast to e4m3 (round-to-nearest-even) as x / s.
+
+    Returns dict(q8, k8, v8 = uint8 code tensors [B, H, N, d]; descale_q, descale_k,
+    descale_v = the scales s as Python floats).  Dequantized value = s * e4m3(code).
+    """
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    out = {}
+    for name, n in (("q", N_q), ("k", N_kv), ("v", N_kv)):
+        x = torch.randn((B, H, n, d), generator=gen, dtype=torch.float32, device=device)
+        amax = float(x.abs().max()) if x.numel() else 1.0
+        s = amax / FP8_E4M3_MAX if amax > 0 else 1.0
+        out[name + "8"] = (x / s).to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
+        out["descale_" + name] = s
+    return out

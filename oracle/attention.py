@@ -328,3 +328,39 @@ def decode(q, k, v, scale: float):
     q [B,H,1,d], k/v [B,H,N_kv,d] -> (O [B,H,1,d], lse [B,H,1]).
     """
     return forward(q, k, v, scale, causal=False)
+
+
+# --------------------------------------------------------------------------------------------
+# FP8 forward
+# --------------------------------------------------------------------------------------------
+# The pages name low precision (FP8) as one of FlashAttention-3's techniques and give no
+# formula for it ([Lesson4] "Causal masks and FlashAttention-3"; [Scratch] "Later versions").
+# Reading taken: Q, K and V arrive as 8-bit e4m3 codes with one scale per tensor, x = s_x * x8,
+# and the result is exact attention of those dequantized tensors.  How the kernel rounds its
+# intermediate weights is the kernel's business; its accuracy bar is set against this result.
+
+def decode_e4m3(codes) -> np.ndarray:
+    """Value of each 8-bit e4m3 code: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits;
+    exponent field 0 is subnormal (m/8 * 2^-6); S.1111.111 is NaN; there is no infinity."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((e == 0xF) & (m == 0x7), np.nan, mag)
+    return sign * mag
+
+
+def forward_fp8(q8, k8, v8, scale: float, descale_q: float, descale_k: float, descale_v: float,
+                causal: bool = False):
+    """Attention of the dequantized tensors s_q Q8, s_k K8, s_v V8 (codes as uint8 arrays or
+    tensors of shape [B, H, N, d]); returns fp64 (O, lse) as ``forward``."""
+    def deq(x, s):
+        try:
+            import torch
+            if isinstance(x, torch.Tensor):
+                x = x.detach().cpu().view(torch.uint8).numpy()
+        except ImportError:  # pragma: no cover
+            pass
+        return decode_e4m3(x) * float(s)
+    return forward(deq(q8, descale_q), deq(k8, descale_k), deq(v8, descale_v), scale, causal)

@@ -367,3 +367,67 @@ def test_merge_is_associative_and_order_free():
     assert abs(l1 - l2) < 1e-13
     w = np.exp(np.array([p[1] for p in parts]) - l1)
     assert abs(w.sum() - 1) < 1e-14                     # merge weights sum to 1
+
+
+# ---------------------------------------------------------------------------- FP8 forward
+# e4m3 codes: 1 sign, 4 exponent (bias 7), 3 mantissa bits; subnormals; S.1111.111 is NaN.
+E4M3_HAND = {0x00: 0.0, 0x80: -0.0, 0x38: 1.0, 0x40: 2.0, 0xC0: -2.0, 0x3C: 1.5, 0x7E: 448.0,
+             0xFE: -448.0, 0x08: 2.0 ** -6, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x30: 0.5,
+             0x77: 240.0, 0x1F: 1.875 * 2.0 ** -4}
+
+
+def test_e4m3_hand_values():
+    for code, val in E4M3_HAND.items():
+        got = A.decode_e4m3(np.array([code]))[0]
+        assert got == val, (hex(code), got, val)
+    assert np.isnan(A.decode_e4m3(np.array([0x7F, 0xFF]))).all()
+
+
+def test_e4m3_all_codes_match_torch_float8():
+    """Every code against an independent decoder (torch's float8_e4m3fn upcast)."""
+    import torch
+    codes = np.arange(256, dtype=np.uint8)
+    mine = A.decode_e4m3(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert (np.isnan(mine) == nan).all()
+    assert np.array_equal(mine[~nan], ref[~nan])
+
+
+def _fp8_case(seed, B=1, H=2, N=40, d=16):
+    g = np.random.default_rng(seed)
+    codes = [g.integers(0, 256, size=(B, H, N, d), dtype=np.uint8) for _ in range(3)]
+    for c in codes:                       # no NaN codes
+        c[(c & 0x7F) == 0x7F] = 0x38
+    return codes
+
+
+def test_forward_fp8_scales_act_where_they_belong():
+    """descale_v scales O and leaves lse; descale_q and descale_k act like the softmax scale;
+    a swapped or dropped scale fails one of these."""
+    q8, k8, v8 = _fp8_case(3)
+    tau = 0.05
+    o1, l1 = A.forward_fp8(q8, k8, v8, tau, 1.0, 1.0, 1.0, causal=True)
+    o2, l2 = A.forward_fp8(q8, k8, v8, tau, 1.0, 1.0, 2.0, causal=True)
+    np.testing.assert_allclose(o2, 2 * o1, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(l2, l1, rtol=1e-13)
+    o3, l3 = A.forward_fp8(q8, k8, v8, tau, 0.5, 1.0, 1.0, causal=True)
+    o4, l4 = A.forward_fp8(q8, k8, v8, tau * 0.5, 1.0, 1.0, 1.0, causal=True)
+    o5, l5 = A.forward_fp8(q8, k8, v8, tau, 1.0, 0.5, 1.0, causal=True)
+    np.testing.assert_allclose(o3, o4, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(o5, o4, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(l3, l4, rtol=1e-12)
+    np.testing.assert_allclose(l5, l4, rtol=1e-12)
+
+
+def test_forward_fp8_equals_torch_sdpa_on_dequantized_values():
+    import torch
+    q8, k8, v8 = _fp8_case(4)
+    sq, sk, sv, tau = 0.02, 0.03, 0.5, 0.25
+    o, lse = A.forward_fp8(q8, k8, v8, tau, sq, sk, sv, causal=False)
+    deq = lambda c, s: torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64) * s
+    qt, kt, vt = deq(q8, sq), deq(k8, sk), deq(v8, sv)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=tau)
+    np.testing.assert_allclose(o, ref.numpy(), rtol=1e-10, atol=1e-12)
+    lse_ref = torch.logsumexp(tau * qt @ kt.transpose(-1, -2), dim=-1)
+    np.testing.assert_allclose(lse, lse_ref.numpy(), rtol=1e-12)

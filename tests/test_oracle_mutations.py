@@ -99,6 +99,29 @@ def _decode_merge_linear_weights(m, l, o):
     return (w[:, None] * np.asarray(o)).sum(axis=0) / l_tot, mm + math.log(l_tot)
 
 
+def _e4m3_bias8(codes):
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e, m = (c >> 3) & 0xF, c & 0x7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 8.0))
+    return sign * np.where((e == 0xF) & (m == 0x7), np.nan, mag)
+
+
+def _e4m3_no_subnormals(codes):
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e, m = (c >> 3) & 0xF, c & 0x7
+    mag = (1.0 + m / 8.0) * np.exp2(e - 7.0)                      # implicit 1 for e == 0 too
+    return sign * np.where((e == 0xF) & (m == 0x7), np.nan, mag)
+
+
+_forward_fp8_orig = A.forward_fp8
+
+
+def _fp8_swapped_scales(q8, k8, v8, scale, dq, dk, dv, causal=False):
+    return _forward_fp8_orig(q8, k8, v8, scale, dv, dk, dq, causal)
+
+
 # the pins each mutation is run against (any failing one is a catch)
 FWD_PINS = [
     lambda: P.test_forward_vs_torch_sdpa_fp64((2, 3, 37, 37, 16), False),
@@ -124,6 +147,13 @@ METHOD_PINS = [
     lambda: P.test_decode_partials_merge_equals_full_row(1000, 7),
 ]
 
+FP8_PINS = [
+    P.test_e4m3_hand_values,
+    P.test_e4m3_all_codes_match_torch_float8,
+    P.test_forward_fp8_scales_act_where_they_belong,
+    P.test_forward_fp8_equals_torch_sdpa_on_dequantized_values,
+]
+
 MUTATIONS = [
     ("scores", _scores_no_scale, FWD_PINS),
     ("scores", _scores_mask(lambda i, j: j < i), FWD_PINS),
@@ -139,6 +169,9 @@ MUTATIONS = [
     ("online_step", _online_step_no_o_rescale, METHOD_PINS),
     ("merge", _merge_plain_average, METHOD_PINS),
     ("decode_merge", _decode_merge_linear_weights, METHOD_PINS),
+    ("decode_e4m3", _e4m3_bias8, FP8_PINS),
+    ("decode_e4m3", _e4m3_no_subnormals, FP8_PINS),
+    ("forward_fp8", _fp8_swapped_scales, FP8_PINS),
 ]
 
 
