@@ -11,6 +11,7 @@ Also measured in the same run and reported in the same JSON line:
   breakdown.*_causal       the causal variant of the workload
   breakdown.decode         split-KV decode (B=64, H=32, N_kv=32768, d=128, 64 splits), GB/s
   breakdown.decode_paged   the same decode over a paged cache (256-key blocks, shuffled), GB/s
+  breakdown.fwd_fp8*       forward from e4m3 Q, K, V (per-tensor scales), same shapes
   roofline                 the dominant kernel of the step (backward main kernel), timed alone
   e2e                      the step through the public Python API with host (pinned) buffers,
                            host->device and device->host copies inside the timed region
@@ -357,6 +358,30 @@ def run_ours(args, rank, world, local_rank):
                                    "ms": round(c_ms, 4)}
     breakdown["fwd_causal"] = {"tflops": round(whole_job_rate(fl_fc, world, cf_ms * 1e-3) / 1e12, 1),
                                "ms": round(cf_ms, 4)}
+
+    # ---- FP8 forward (e4m3 Q, K, V with per-tensor scales) on the same shapes
+    x8 = inputs.make_qkv_fp8(w.B, w.H, w.N_q, w.N_kv, w.d, w.seed + 7919 * rank, device=str(dev))
+    peak_f8 = 2 * peak_tf                    # nominal fp8 : bf16 dense ratio of 2 on this part
+
+    def fwd8(causal):
+        def f(pe):
+            if pe is not None:
+                pe[0].record(stream)
+            fa.fa_fwd_fp8(x8["q8"], x8["k8"], x8["v8"], d["o"], d["lse"], w.scale, x8["descale_q"],
+                          x8["descale_k"], x8["descale_v"], causal)
+            if pe is not None:
+                pe[1].record(stream)
+        return f
+    for causal, key, fl in ((False, "fwd_fp8", fl_f), (True, "fwd_fp8_causal", fl_fc)):
+        t8, i8 = timed(fwd8(causal), K, inner=True)
+        ms8 = reduce_max(t8 / K)
+        k8 = statistics.mean(i8)
+        breakdown[key] = {"tflops": round(whole_job_rate(fl, world, ms8 * 1e-3) / 1e12, 1),
+                          "ms": round(ms8, 4), "kernel_ms": round(k8, 4),
+                          "frac_of_fp8_peak": round(fl / (k8 * 1e-3) / 1e12 / peak_f8, 4),
+                          "fp8_peak": peak_f8,
+                          "peak_source": "2 x bf16_tflops (burst, measured): nominal fp8/bf16 ratio"}
+    del x8
 
     # ---- e2e through the public API with pinned host buffers (restore the headline inputs)
     host = {k_: x[k_].pin_memory() for k_ in ("q", "k", "v", "do")}

@@ -19,7 +19,7 @@ __all__ = [
     "fa_fwd", "fa_bwd", "fa_bwd_prep", "fa_bwd_main", "fa_bwd_finish", "fa_decode_splitkv", "fa_bwd_workspace_size", "fa_decode_splitkv_noalloc",
     "fa_decode_workspace_size", "fa_sync_status", "fa_status_string", "fa_last_error_message",
     "forward", "backward", "decode", "fa_fwd_varlen", "forward_varlen",
-    "fa_bwd_varlen", "backward_varlen", "fa_decode_paged", "decode_paged",
+    "fa_bwd_varlen", "backward_varlen", "fa_decode_paged", "decode_paged", "fa_fwd_fp8", "forward_fp8",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -60,6 +60,7 @@ _SIGNATURES = {
     "fa_decode_workspace_size": (_S, [_I, _I, _I, _I, _I]),
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
     "fa_decode_splitkv_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _F, _F, _I, _P]),
     "fa_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S,
                              _P]),
     "fa_sync_status": (_I, [_P]),
@@ -229,6 +230,16 @@ def fa_decode_splitkv_noalloc(q, k, v, o, lse, scale: float, n_splits: int, stre
                                                     _stream(stream)))
 
 
+def fa_fwd_fp8(q8, k8, v8, o, lse, scale: float, descale_q: float, descale_k: float,
+               descale_v: float, causal: bool = False, stream=None):
+    """q8, k8, v8: e4m3 codes (uint8 or float8_e4m3fn tensors) [B,H,N,d]; o bf16, lse fp32."""
+    B, H, n_q, d = q8.shape
+    n_kv = k8.shape[2]
+    _check(load_library().fa_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(o), _ptr(lse), B, H, n_q,
+                                     n_kv, d, float(scale), float(descale_q), float(descale_k),
+                                     float(descale_v), int(bool(causal)), _stream(stream)))
+
+
 def fa_decode_paged(q, k_cache, v_cache, o, lse, block_table, seqlens_k, max_seqlen_k: int,
                     scale: float, n_splits: int, ws, stream=None):
     """q [B,H,1,d]; k/v cache [num_blocks, block_size, H, d]; block_table [B, max_blocks] int32;
@@ -318,4 +329,16 @@ def decode_paged(q, k_cache, v_cache, block_table, seqlens_k, max_seqlen_k: int,
     lse = torch.empty((B, H, 1), dtype=torch.float32, device=q.device)
     fa_decode_paged(q, k_cache, v_cache, o, lse, block_table, seqlens_k, max_seqlen_k, scale,
                     n_splits, workspace, stream)
+    return o, lse
+
+
+def forward_fp8(q8, k8, v8, descale_q: float, descale_k: float, descale_v: float,
+                causal: bool = False, scale: float | None = None, stream=None):
+    """FP8 forward -> (O bf16 [B,H,N_q,d], lse fp32 [B,H,N_q])."""
+    import torch
+    B, H, n_q, d = q8.shape
+    scale = d ** -0.5 if scale is None else scale
+    o = torch.empty((B, H, n_q, d), dtype=torch.bfloat16, device=q8.device)
+    lse = torch.empty((B, H, n_q), dtype=torch.float32, device=q8.device)
+    fa_fwd_fp8(q8, k8, v8, o, lse, scale, descale_q, descale_k, descale_v, causal, stream)
     return o, lse

@@ -83,6 +83,36 @@ fa_status_t fa_fwd(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v, f
   return FA_OK;
 }
 
+fa_status_t fa_fwd_fp8(const fa_e4m3_t* q, const fa_e4m3_t* k, const fa_e4m3_t* v, fa_bf16_t* o,
+                       float* lse, int B, int H, int N_q, int N_kv, int d, float scale,
+                       float descale_q, float descale_k, float descale_v, int causal,
+                       void* stream) {
+  fa_status_t st = check_shape(B, H, N_q, N_kv, d, scale);
+  if (st != FA_OK) return st;
+  if (d != 128) return fail(FA_ERR_UNSUPPORTED, "the fp8 forward supports d = 128 only (got %d)", d);
+  for (float ds : {descale_q, descale_k, descale_v})
+    if (!std::isfinite(ds) || !(ds > 0.f))
+      return fail(FA_ERR_INVALID_ARG, "descale factors must be finite and > 0 (got %g)",
+                  static_cast<double>(ds));
+  if (!std::isfinite(scale * descale_q * descale_k) || !(scale * descale_q * descale_k > 0.f))
+    return fail(FA_ERR_INVALID_ARG, "scale * descale_q * descale_k must be a finite positive float");
+  if (causal && N_q != N_kv)
+    return fail(FA_ERR_UNSUPPORTED, "causal requires N_q == N_kv (got %d, %d)", N_q, N_kv);
+  if (N_q == 0) return FA_OK;
+  if (!q || !o || !lse || (N_kv > 0 && (!k || !v)))
+    return fail(FA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(FA_ERR_INVALID_ARG, "arrays must be 16-byte aligned");
+  fa::FwdArgs a{q, k ? k : q, v ? v : q, o, lse, B, H, N_q, N_kv, d, scale, causal ? 1 : 0};
+  if (N_kv == 0) { a.k = q; a.v = q; }
+  a.descale_q = descale_q;
+  a.descale_k = descale_k;
+  a.descale_v = descale_v;
+  cudaError_t e = fa::launch_fwd_fp8(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_fp8 launch");
+  return FA_OK;
+}
+
 fa_status_t fa_fwd_varlen(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
                           fa_bf16_t* o, float* lse, const int* cu_seqlens_q,
                           const int* cu_seqlens_k, int n_seqs, int H, int total_q, int total_k,

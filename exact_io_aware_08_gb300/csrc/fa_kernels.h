@@ -25,6 +25,7 @@ struct FwdArgs {
   int B, H, n_q, n_kv, d;
   float scale;
   int causal;
+  float descale_q = 1.f, descale_k = 1.f, descale_v = 1.f;   // fp8 forward only
 };
 
 struct FwdVarlenArgs {
@@ -90,6 +91,7 @@ struct DecodePagedArgs {
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream);   // d = 128 only
 cudaError_t launch_fwd_varlen(const FwdVarlenArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_prep(const BwdArgs& a, cudaStream_t stream);    // F2
 cudaError_t launch_bwd_main(const BwdArgs& a, cudaStream_t stream);    // F3

@@ -35,18 +35,29 @@
 
 namespace fa {
 
-template <int D>
+template <int D, bool F8 = false>
 struct FwdCfg {
+  static_assert(!F8 || D == 128, "the fp8 forward is built for d = 128");
+  static constexpr int EB = F8 ? 1 : 2;               // bytes per Q/K/V element
   static constexpr int BM = 128;                      // rows per query tile (2 tiles per CTA)
   static constexpr int BN = 128;                      // keys per K/V tile
-  static constexpr int KCH = D / 64;                  // 64-column (128-byte) chunks per row
-  static constexpr int TILE = 128 * D * 2;            // bytes of one 128-row bf16 tile
-  static constexpr int CHUNK = 128 * 128;             // bytes of one [128 x 64] swizzled chunk
-  static constexpr int NS = (D == 128) ? 2 : 4;       // K ring and V ring depth
-  static constexpr int OFF_Q = 0;                     // Q_0, Q_1 (later: O staging)
+  static constexpr int KCH = D * EB / 128;            // 128-byte chunks per Q/K/V row
+  static constexpr int XCH = 128 / EB;                // elements per chunk (TMA x step)
+  static constexpr int TILE = 128 * D * EB;           // bytes of one 128-row Q/K/V tile
+  static constexpr int CHUNK = 128 * 128;             // bytes of one [128 rows x 128 B] chunk
+  static constexpr int OCH = D / 64;                  // 64-column chunks of a bf16 O row
+  static constexpr int OTILE = 128 * D * 2;           // bytes of one 128-row bf16 O tile
+  static constexpr int NS = F8 ? 3 : ((D == 128) ? 2 : 4);   // K ring and V ring depth
+  static constexpr int KS_S = D * EB / 32;            // 32-byte k-steps of S = Q K^T
+  static constexpr int KS_PV = BN * EB / 32;          // 32-byte k-steps of O += P V
+  static constexpr int PV_B_STEP = (32 / EB) * 128;   // V bytes per PV k-step (32/EB key rows)
+  static constexpr int P_COLS = BN * EB / 4;          // TMEM columns P occupies over S
+  static constexpr int OFF_Q = 0;                     // Q_0, Q_1 (bf16: later O staging)
   static constexpr int OFF_K = 2 * TILE;
   static constexpr int OFF_V = OFF_K + NS * TILE;
-  static constexpr int OFF_BAR = OFF_V + NS * TILE;
+  // O staging: the dead Q tiles when they are as large as O tiles (bf16), else its own space
+  static constexpr int OFF_OST = F8 ? OFF_V + NS * TILE : OFF_Q;
+  static constexpr int OFF_BAR = F8 ? OFF_OST + 2 * OTILE : OFF_V + NS * TILE;
   // q_full, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[2], p_full[2], o_done[2]
   static constexpr int NBAR = 1 + 4 * NS + 6;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
@@ -59,7 +70,12 @@ struct FwdCfg {
   // MMA) drops to 80, the two softmax warpgroups rise to 208: 128*80 + 2*128*208 = 63488.
   static constexpr uint32_t REG_CTRL = 80;
   static constexpr uint32_t REG_SOFTMAX = 208;
-  static constexpr float RESCALE_THRESHOLD = 8.f;     // log2 units: factor 256
+  // Weights are 2^{(s - m) c2 + P_BIAS} with m at most RESCALE_THRESHOLD (log2 units) below
+  // the row's running max, so they stay <= 2^{P_BIAS + RESCALE_THRESHOLD} = 256: exact in fp32
+  // for bf16; for e4m3 (largest finite 448) the bias lifts small weights out of the subnormal
+  // range (e4m3 is normal down to 2^-6).
+  static constexpr float RESCALE_THRESHOLD = F8 ? 4.f : 8.f;
+  static constexpr float P_BIAS = F8 ? 4.f : 0.f;
 };
 
 struct FwdParams {
@@ -73,12 +89,15 @@ struct FwdParams {
   const int* cu_q;
   const int* cu_k;
   uint16_t* o;                                        // for row-wise stores of a partial tile
+  // FP8: scale = tau * s_q * s_k (the score scale of the raw code products); O is multiplied by
+  // out_scale = s_v.  bf16: out_scale = 1.
+  float out_scale;
 };
 
-template <int D, bool VL>
-__global__ void __launch_bounds__(FwdCfg<D>::THREADS, 1)
+template <int D, bool VL, bool F8 = false>
+__global__ void __launch_bounds__(FwdCfg<D, F8>::THREADS, 1)
 fwd_kernel(const __grid_constant__ FwdParams p) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem_1k(smem_raw);
   uint8_t* sQ = smem + C::OFF_Q;
@@ -173,18 +192,18 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       mbar_arrive_expect_tx(q_full, nq_tiles * C::TILE);
       for (int t = 0; t < nq_tiles; ++t)
         for (int k = 0; k < C::KCH; ++k)
-          tma_load_3d(sQ + t * C::TILE + k * C::CHUNK, &p.tq, q_full, k * 64, y1(q0[t]), y2(q_beg, q0[t]));
+          tma_load_3d(sQ + t * C::TILE + k * C::CHUNK, &p.tq, q_full, k * C::XCH, y1(q0[t]), y2(q_beg, q0[t]));
       for (int j = 0; j < n_max; ++j) {
         const int s = j % C::NS;
         const uint32_t u = j / C::NS;
         if (u > 0 && !mbar_wait(&k_empty[s], (u - 1) & 1, abort_flag, 101)) break;
         mbar_arrive_expect_tx(&k_full[s], C::TILE);
         for (int k = 0; k < C::KCH; ++k)
-          tma_load_3d(sK + s * C::TILE + k * C::CHUNK, &p.tk, &k_full[s], k * 64, y1(j * C::BN), y2(k_beg, j * C::BN));
+          tma_load_3d(sK + s * C::TILE + k * C::CHUNK, &p.tk, &k_full[s], k * C::XCH, y1(j * C::BN), y2(k_beg, j * C::BN));
         if (u > 0 && !mbar_wait(&v_empty[s], (u - 1) & 1, abort_flag, 102)) break;
         mbar_arrive_expect_tx(&v_full[s], C::TILE);
         for (int k = 0; k < C::KCH; ++k)
-          tma_load_3d(sV + s * C::TILE + k * C::CHUNK, &p.tv, &v_full[s], k * 64, y1(j * C::BN), y2(k_beg, j * C::BN));
+          tma_load_3d(sV + s * C::TILE + k * C::CHUNK, &p.tv, &v_full[s], k * C::XCH, y1(j * C::BN), y2(k_beg, j * C::BN));
         issued = j + 1;
       }
       if (*abort_flag) {
@@ -199,8 +218,9 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_max > 0) {
-      const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
-      const uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);    // P from TMEM, V MN-major
+      // Q, K both K-major; P from TMEM, V MN-major
+      const uint32_t idesc_s = F8 ? idesc_e4m3_f32(128, 128, 0, 0) : idesc_bf16_f32(128, 128, 0, 0);
+      const uint32_t idesc_o = F8 ? idesc_e4m3_f32(128, D, 0, 1) : idesc_bf16_f32(128, D, 0, 1);
       // Descriptors are built once; each k-step adds a compile-time offset (desc_advance).
       const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 0, 1024);
       const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 0, 1024);
@@ -210,9 +230,12 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
         const uint64_t b = desc_advance(dk0, (j % C::NS) * C::TILE);
         const uint32_t d_tmem = tbase + C::T_S + t * 128;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
+        for (int ks = 0; ks < C::KS_S; ++ks) {
           const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
-          umma_ss(d_tmem, desc_advance(a, off), desc_advance(b, off), idesc_s, ks > 0);
+          if constexpr (F8)
+            umma_ss_f8(d_tmem, desc_advance(a, off), desc_advance(b, off), idesc_s, ks > 0);
+          else
+            umma_ss(d_tmem, desc_advance(a, off), desc_advance(b, off), idesc_s, ks > 0);
         }
         umma_commit(&s_full[t]);
       };
@@ -221,9 +244,14 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
         const uint32_t d_tmem = tbase + C::T_O + t * D;
         const uint32_t a_tmem = tbase + C::T_S + t * 128;
 #pragma unroll
-        for (int ks = 0; ks < C::BN / 16; ++ks)
-          umma_ts(d_tmem, a_tmem + ks * 8, desc_advance(b, ks * 2048), idesc_o,
-                  (j > 0 || ks > 0) ? 1u : 0u);
+        for (int ks = 0; ks < C::KS_PV; ++ks) {
+          if constexpr (F8)
+            umma_ts_f8(d_tmem, a_tmem + ks * 8, desc_advance(b, ks * C::PV_B_STEP), idesc_o,
+                       (j > 0 || ks > 0) ? 1u : 0u);
+          else
+            umma_ts(d_tmem, a_tmem + ks * 8, desc_advance(b, ks * C::PV_B_STEP), idesc_o,
+                    (j > 0 || ks > 0) ? 1u : 0u);
+        }
       };
       bool ok = mbar_wait(q_full, 0, abort_flag, 111) && mbar_wait(&k_full[0], 0, abort_flag, 112);
       if (ok) {
@@ -335,11 +363,27 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
           }
         }
       }
-      const float ms = (m == -INFINITY) ? 0.f : m * c2;
+      const float ms = (m == -INFINITY) ? 0.f : m * c2 - C::P_BIAS;
       const float2 c2v = make_float2(c2, c2), nms = make_float2(-ms, -ms);
       float2 rs[4], rb[4];                      // independent partial sums (ILP)
 #pragma unroll
       for (int g = 0; g < 4; ++g) rs[g] = rb[g] = make_float2(0.f, 0.f);
+      if constexpr (F8) {
+        // P as e4m3, four weights per column, over the first 32 columns of S_t.  O is
+        // normalised by the fp32 sum l: e4m3 rounding (relative 2^-4, to nearest) of each
+        // weight perturbs O by a zero-mean sum, bounded by 2^-4 sum_j p_j |v_j| / l.
+        uint32_t pk[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float2 x0 = ffma2(make_float2(s[4 * k], s[4 * k + 1]), c2v, nms);
+          const float2 x1 = ffma2(make_float2(s[4 * k + 2], s[4 * k + 3]), c2v, nms);
+          const float2 e0 = make_float2(fast_exp2(x0.x), fast_exp2(x0.y));
+          const float2 e1 = make_float2(fast_exp2(x1.x), fast_exp2(x1.y));
+          pk[k] = pack_e4m3x4(e0.x, e0.y, e1.x, e1.y);
+          rs[k & 3] = fadd2(rs[k & 3], fadd2(e0, e1));
+        }
+        tmem_st32(t_s, pk);
+      } else {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {             // P over the first 64 columns of S_t, 2 halves
         uint32_t pk[32];
@@ -357,6 +401,7 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
         }
         tmem_st32(t_s + h * 32, pk);
       }
+      }
       const float2 rs01 = fadd2(fadd2(rs[0], rs[1]), fadd2(rs[2], rs[3]));
       const float2 rb01 = fadd2(fadd2(rb[0], rb[1]), fadd2(rb[2], rb[3]));
       l += rs01.x + rs01.y;
@@ -371,13 +416,13 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       ok = mbar_wait_warp(&o_done[t], 0, abort_flag, 123);
       tc_fence_after();
     }
-    uint8_t* stage = sQ + t * C::TILE;         // Q_t is dead once o_done[t] fired
+    uint8_t* stage = smem + C::OFF_OST + t * C::OTILE;   // bf16: Q_t, dead once o_done[t] fired
     // A packed tile that ends past its sequence is stored row by row (a TMA store of the
     // whole box would write into the next sequence's rows).
     const bool rowwise = VL && (q0[t] + C::BM > n_q);
     uint16_t* orow = rowwise ? p.o + (static_cast<size_t>(q_beg + q_idx) * p.heads + head) * D : nullptr;
     if (ok && q0[t] < n_q) {
-      const float inv_l = (lb > 0.f) ? 1.f / lb : 0.f;
+      const float inv_l = F8 ? ((l > 0.f) ? p.out_scale / l : 0.f) : ((lb > 0.f) ? 1.f / lb : 0.f);
 #pragma unroll
       for (int k = 0; k < D / 32; ++k) {
         uint32_t rr[32];
@@ -406,13 +451,14 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       if (q_idx < n_q) {
         const size_t li = VL ? static_cast<size_t>(head) * p.total_q + q_beg + q_idx
                                    : static_cast<size_t>(bh) * n_q + q_idx;
-        p.lse[li] = (l > 0.f) ? fmaf(m, p.scale, logf(l)) : -INFINITY;
+        // l carries the factor 2^P_BIAS of the weights
+        p.lse[li] = (l > 0.f) ? fmaf(m, p.scale, logf(l) - C::P_BIAS * 0.6931471805599453f) : -INFINITY;
       }
       fence_proxy_async_smem();
     }
     named_bar_sync(1 + t, 128);
     if (ok && !rowwise && q0[t] < n_q && (threadIdx.x & 127) == 64) {
-      for (int k = 0; k < C::KCH; ++k)
+      for (int k = 0; k < C::OCH; ++k)
         tma_store_3d(&p.to, stage + k * C::CHUNK, k * 64, y1(q0[t]), y2(q_beg, q0[t]));
       bulk_commit_group();
       bulk_wait_group_read0();
@@ -454,6 +500,7 @@ static cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   p.total_q = 0;
   p.cu_q = p.cu_k = nullptr;
   p.o = static_cast<uint16_t*>(a.o);
+  p.out_scale = 1.f;
   static int attr_done[64] = {0};   // one per instantiation of this launcher
   cudaError_t e = ensure_smem_attr(fwd_kernel<D, false>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
@@ -488,12 +535,47 @@ static cudaError_t launch_fwd_varlen_d(const FwdVarlenArgs& a, cudaStream_t stre
   p.cu_q = a.cu_q;
   p.cu_k = a.cu_k;
   p.o = static_cast<uint16_t*>(a.o);
+  p.out_scale = 1.f;
   static int attr_done[64] = {0};
   cudaError_t e = ensure_smem_attr(fwd_kernel<D, true>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
   const uint64_t grid = static_cast<uint64_t>(p.n_qpairs) * a.n_seqs * a.H;
   if (grid == 0) return cudaSuccess;
   fwd_kernel<D, true><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// FP8 forward (d = 128): e4m3 Q, K, V with one scale each; bf16 O, fp32 lse.
+cudaError_t launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream) {
+  constexpr int D = 128;
+  using C = FwdCfg<D, true>;
+  FwdParams p;
+  const uint64_t bh = static_cast<uint64_t>(a.B) * a.H;
+  const uint64_t kv_rows = a.n_kv > 0 ? static_cast<uint64_t>(a.n_kv) : 1;
+  const uint64_t kv_planes = a.n_kv > 0 ? bh : 1;
+  if (!make_map_u8_3d(&p.tq, a.q, D, a.n_q, bh, 128, 128) ||
+      !make_map_u8_3d(&p.tk, a.k, D, kv_rows, kv_planes, 128, 128) ||
+      !make_map_u8_3d(&p.tv, a.v, D, kv_rows, kv_planes, 128, 128) ||
+      !make_map_bf16_3d(&p.to, a.o, D, a.n_q, bh, 64, 128))
+    return cudaErrorInvalidValue;
+  p.lse = a.lse;
+  p.n_q = a.n_q;
+  p.n_kv = a.n_kv;
+  p.n_qpairs = (a.n_q + 2 * C::BM - 1) / (2 * C::BM);
+  p.n_kvtiles = (a.n_kv + C::BN - 1) / C::BN;
+  p.causal = a.causal;
+  p.scale = a.scale * a.descale_q * a.descale_k;
+  p.scale_log2 = p.scale * 1.4426950408889634f;
+  p.heads = a.H;
+  p.total_q = 0;
+  p.cu_q = p.cu_k = nullptr;
+  p.o = static_cast<uint16_t*>(a.o);
+  p.out_scale = a.descale_v;
+  static int attr_done[64] = {0};
+  cudaError_t e = ensure_smem_attr(fwd_kernel<D, false, true>, C::SMEM_BYTES, attr_done);
+  if (e != cudaSuccess) return e;
+  const uint64_t grid = static_cast<uint64_t>(p.n_qpairs) * bh;
+  fwd_kernel<D, false, true><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 

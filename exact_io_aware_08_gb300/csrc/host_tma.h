@@ -43,6 +43,22 @@ inline bool make_map_bf16_3d(CUtensorMap* map, const void* base, uint64_t inner,
   return r == CUDA_SUCCESS;
 }
 
+// 8-bit tensor {inner, rows, planes} (e4m3 codes) with dense strides; box {box_inner, box_rows, 1}
+// in bytes; 128-byte swizzle (box_inner <= 128).
+inline bool make_map_u8_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                           uint64_t planes, uint32_t box_inner, uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {inner, rows, planes};
+  const cuuint64_t strides[2] = {inner, inner * rows};
+  const cuuint32_t box[3] = {box_inner, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Packed token-major bf16 tensor [total, H, d] as {d, H, total}: box {box_inner, 1, box_rows}
 // covers box_rows consecutive tokens of one head and lands in shared memory exactly like the
 // [B, H, N, d] box above.

@@ -235,6 +235,27 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// 8-bit variants (kind::f8f6f4, A and B both e4m3 here): one instruction consumes K = 32, i.e.
+// the same 32 bytes of a K-major row as a K = 16 bf16 step; from TMEM, A packs four K elements
+// per 32-bit column (lowest K in the lowest byte), so one K = 32 step also covers 8 columns.
+__device__ __forceinline__ void umma_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "setp.ne.b32 P, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, P;\n\t}"
+      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+__device__ __forceinline__ void umma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "setp.ne.b32 P, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, P;\n\t}"
+      :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
 // Arrive once on ``bar`` when all previously issued tcgen05.mma of this thread complete.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
@@ -338,6 +359,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int a_mn, in
        | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// kind::f8f6f4 with A = B = e4m3 (format code 0 for both), fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4)                                  // D format: f32
+       | (0u << 7)                                  // A format: e4m3
+       | (0u << 10)                                 // B format: e4m3
+       | (static_cast<uint32_t>(a_mn) << 15)
+       | (static_cast<uint32_t>(b_mn) << 16)
+       | (static_cast<uint32_t>(N >> 3) << 17)
+       | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // Byte offset of element (row, col) inside a [rows x 64] bf16 tile stored with the 128-byte
 // swizzle (the layout TMA writes for a box whose inner extent is 64 bf16): 16-byte chunk index
 // XORed with (row mod 8).
@@ -394,6 +426,18 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Four fp32 values rounded (to nearest, saturating at +-448) to e4m3 and packed into one
+// 32-bit word, a0 in the lowest byte.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a0, float a1, float a2, float a3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r) : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
   return r;
 }
 

@@ -37,6 +37,7 @@ extern "C" {
 #endif
 
 typedef uint16_t fa_bf16_t; /* raw bfloat16 bits */
+typedef uint8_t fa_e4m3_t;  /* raw 8-bit float code: 1 sign, 4 exponent (bias 7), 3 mantissa bits */
 
 typedef enum {
   FA_OK = 0,
@@ -62,6 +63,26 @@ typedef enum {
 fa_status_t fa_fwd(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v, fa_bf16_t* o,
                    float* lse, int B, int H, int N_q, int N_kv, int d, float scale, int causal,
                    void* stream);
+
+/*
+ * fa_fwd_fp8 -- attention forward from 8-bit inputs (the low-precision FP8 path [Lesson4]
+ * "Causal masks and FlashAttention-3" and [Scratch] "Later versions" name; the pages give no
+ * formula, so this follows the plainest reading: one scale per tensor).
+ *
+ *   Q = descale_q * Q8, K = descale_k * K8, V = descale_v * V8   (Q8, K8, V8: e4m3 codes)
+ *   O, lse = fa_fwd(Q, K, V) with the given scale                bf16 O, fp32 lse
+ *
+ * q, k, v: [B,H,N,d] e4m3 codes; o, lse as for fa_fwd.  d must be 128.  Scores accumulate in
+ * fp32 from exact code products; the attention weights are rounded to e4m3 for the P V product
+ * (the tensor core's 8-bit kind takes both operands in 8 bits), so O differs from the exact
+ * result by at most 2^-4 * sum_j P_ij |V_j| (plus bf16 output rounding), and by much less on
+ * average (the roundings are to nearest and independent); lse uses the unrounded weights.
+ * scale, descale_* must be finite and > 0; other rules as for fa_fwd.
+ */
+fa_status_t fa_fwd_fp8(const fa_e4m3_t* q, const fa_e4m3_t* k, const fa_e4m3_t* v, fa_bf16_t* o,
+                       float* lse, int B, int H, int N_q, int N_kv, int d, float scale,
+                       float descale_q, float descale_k, float descale_v, int causal,
+                       void* stream);
 
 /*
  * fa_fwd_varlen -- attention forward over a batch of sequences of different lengths, packed

@@ -139,3 +139,17 @@ def test_paged_decode_rejection(lib):
     assert call(d=80) == UNSUPPORTED
     assert call(ws_bytes=2 * 2 * 4 * 130 * 4 - 4) == WORKSPACE
     assert call(num_blocks=1 << 24, block_size=256) == UNSUPPORTED   # rows past 2^31
+
+
+def test_fwd_fp8_rejection(lib):
+    def call(d=128, scale=0.1, dq=0.01, dk=0.01, dv=0.01, causal=0, N_kv=256, k=FAKE):
+        return lib.fa_fwd_fp8(FAKE, k, FAKE, FAKE, FAKE, 1, 2, 256, N_kv, d, scale, dq, dk, dv,
+                              causal, None)
+    assert call(d=64) == UNSUPPORTED
+    assert call(dq=0.0) == INVALID
+    assert call(dv=float("nan")) == INVALID
+    assert call(dk=-1.0) == INVALID
+    assert call(scale=float("inf")) == INVALID
+    assert call(dq=1e-30, dk=1e-30) == INVALID          # the product underflows to 0
+    assert call(causal=1, N_kv=128) == UNSUPPORTED
+    assert call(k=FAKE + 8) == INVALID
