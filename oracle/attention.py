@@ -364,3 +364,61 @@ def forward_fp8(q8, k8, v8, scale: float, descale_q: float, descale_k: float, de
             pass
         return decode_e4m3(x) * float(s)
     return forward(deq(q8, descale_q), deq(k8, descale_k), deq(v8, descale_v), scale, causal)
+
+
+# --------------------------------------------------------------------------------------------
+# Sliding-window attention
+# --------------------------------------------------------------------------------------------
+# The pages name sliding-window masks, next to causal ones, as what long-context training uses,
+# with the same tile skipping ([Lesson4] section 6 "Where it shows up", Training).  Reading
+# taken: query i sees key j iff i - left <= j <= i + right, over one sequence (N_q == N_kv); a
+# negative bound is unbounded on that side, so (left, right) = (-1, 0) is the causal mask and
+# (-1, -1) no mask.  Everything else is the plain definition with those scores at -inf.
+
+def window_visible(n_q: int, n_kv: int, left: int, right: int) -> np.ndarray:
+    """Boolean [n_q, n_kv]: True where key j is inside query i's window."""
+    i = np.arange(n_q)[:, None]
+    j = np.arange(n_kv)[None, :]
+    vis = np.ones((n_q, n_kv), dtype=bool)
+    if left >= 0:
+        vis &= j >= i - left
+    if right >= 0:
+        vis &= j <= i + right
+    return vis
+
+
+def forward_window_head(q, k, v, scale: float, left: int, right: int):
+    """One head under a sliding window: returns (O, lse, P)."""
+    s = scale * (q @ k.T)
+    s = np.where(window_visible(q.shape[0], k.shape[0], left, right), s, NEG_INF)
+    p, m, l = three_pass_softmax(s)
+    return p @ v, lse_from(m, l), p
+
+
+def forward_window(q, k, v, scale: float, left: int, right: int):
+    """Sliding-window forward over [B, H, N, d]; fp64 (O, lse)."""
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    B, H, n_q, d = q.shape
+    o = np.zeros((B, H, n_q, v.shape[-1]))
+    lse = np.full((B, H, n_q), NEG_INF)
+    for b in range(B):
+        for h in range(H):
+            o[b, h], lse[b, h], _ = forward_window_head(q[b, h], k[b, h], v[b, h], scale, left, right)
+    return o, lse
+
+
+def backward_window(q, k, v, do, scale: float, left: int, right: int):
+    """Sliding-window gradients: the backward formulas of ``backward_head`` with the window's P
+    (masked scores have P = 0, so they contribute nothing)."""
+    q, k, v, do = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(do)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(q.shape[0]):
+        for h in range(q.shape[1]):
+            _, _, p = forward_window_head(q[b, h], k[b, h], v[b, h], scale, left, right)
+            dv[b, h] = p.T @ do[b, h]
+            dp = do[b, h] @ v[b, h].T
+            D = (p * dp).sum(axis=-1)
+            ds = p * (dp - D[:, None])
+            dq[b, h] = scale * (ds @ k[b, h])
+            dk[b, h] = scale * (ds.T @ q[b, h])
+    return dq, dk, dv

@@ -431,3 +431,62 @@ def test_forward_fp8_equals_torch_sdpa_on_dequantized_values():
     np.testing.assert_allclose(o, ref.numpy(), rtol=1e-10, atol=1e-12)
     lse_ref = torch.logsumexp(tau * qt @ kt.transpose(-1, -2), dim=-1)
     np.testing.assert_allclose(lse, lse_ref.numpy(), rtol=1e-12)
+
+
+# ---------------------------------------------------------------------------- sliding window
+def _qkv(seed, B=1, H=2, N=37, d=8):
+    g = np.random.default_rng(seed)
+    return [g.standard_normal((B, H, N, d)) for _ in range(4)]
+
+
+def test_window_special_cases_reduce_to_causal_and_full():
+    q, k, v, _ = _qkv(1)
+    for (left, right), causal in (((-1, 0), True), ((-1, -1), False), ((40, 40), False), ((36, 0), True)):
+        o, lse = A.forward_window(q, k, v, 0.3, left, right)
+        o_ref, lse_ref = A.forward(q, k, v, 0.3, causal)
+        np.testing.assert_allclose(o, o_ref, atol=1e-14)
+        np.testing.assert_allclose(lse, lse_ref, atol=1e-13)
+
+
+def test_window_zero_width_returns_own_value():
+    q, k, v, _ = _qkv(2)
+    o, lse = A.forward_window(q, k, v, 0.3, 0, 0)
+    np.testing.assert_array_equal(o, v)
+    np.testing.assert_allclose(lse, 0.3 * np.einsum("bhnd,bhnd->bhn", q, k), atol=1e-14)
+
+
+@pytest.mark.parametrize("left,right", [(5, 0), (3, 7), (0, 4), (10, -1)])
+def test_window_vs_torch_sdpa_boolean_mask(left, right):
+    import torch
+    q, k, v, _ = _qkv(3)
+    o, lse = A.forward_window(q, k, v, 0.3, left, right)
+    N = q.shape[2]
+    i = torch.arange(N)[:, None]
+    j = torch.arange(N)[None, :]
+    mask = torch.ones(N, N, dtype=torch.bool)
+    if left >= 0:
+        mask &= j >= i - left
+    if right >= 0:
+        mask &= j <= i + right
+    qt, kt, vt = (torch.from_numpy(t) for t in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=0.3)
+    np.testing.assert_allclose(o, ref.numpy(), atol=1e-13)
+    s = (0.3 * qt @ kt.transpose(-1, -2)).masked_fill(~mask, float("-inf"))
+    np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).numpy(), atol=1e-13)
+
+
+@pytest.mark.parametrize("left,right", [(6, 0), (2, 5)])
+def test_window_backward_vs_torch_autograd(left, right):
+    import torch
+    q, k, v, do = _qkv(4, N=29)
+    dq, dk, dv = A.backward_window(q, k, v, do, 0.3, left, right)
+    N = q.shape[2]
+    i = torch.arange(N)[:, None]
+    j = torch.arange(N)[None, :]
+    mask = (j >= i - left) & ((j <= i + right) if right >= 0 else torch.ones_like(j, dtype=torch.bool))
+    qt, kt, vt = (torch.from_numpy(t).requires_grad_() for t in (q, k, v))
+    out = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=0.3)
+    out.backward(torch.from_numpy(do))
+    np.testing.assert_allclose(dq, qt.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dk, kt.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dv, vt.grad.numpy(), atol=1e-12)

@@ -122,6 +122,28 @@ def _fp8_swapped_scales(q8, k8, v8, scale, dq, dk, dv, causal=False):
     return _forward_fp8_orig(q8, k8, v8, scale, dv, dk, dq, causal)
 
 
+def _window_off_by_one(n_q, n_kv, left, right):
+    i = np.arange(n_q)[:, None]
+    j = np.arange(n_kv)[None, :]
+    vis = np.ones((n_q, n_kv), dtype=bool)
+    if left >= 0:
+        vis &= j > i - left                                      # drops the window's first key
+    if right >= 0:
+        vis &= j <= i + right
+    return vis
+
+
+def _window_sides_swapped(n_q, n_kv, left, right):
+    i = np.arange(n_q)[:, None]
+    j = np.arange(n_kv)[None, :]
+    vis = np.ones((n_q, n_kv), dtype=bool)
+    if right >= 0:
+        vis &= j >= i - right
+    if left >= 0:
+        vis &= j <= i + left
+    return vis
+
+
 # the pins each mutation is run against (any failing one is a catch)
 FWD_PINS = [
     lambda: P.test_forward_vs_torch_sdpa_fp64((2, 3, 37, 37, 16), False),
@@ -154,6 +176,13 @@ FP8_PINS = [
     P.test_forward_fp8_equals_torch_sdpa_on_dequantized_values,
 ]
 
+WINDOW_PINS = [
+    P.test_window_special_cases_reduce_to_causal_and_full,
+    P.test_window_zero_width_returns_own_value,
+    lambda: P.test_window_vs_torch_sdpa_boolean_mask(3, 7),
+    lambda: P.test_window_backward_vs_torch_autograd(2, 5),
+]
+
 MUTATIONS = [
     ("scores", _scores_no_scale, FWD_PINS),
     ("scores", _scores_mask(lambda i, j: j < i), FWD_PINS),
@@ -172,6 +201,8 @@ MUTATIONS = [
     ("decode_e4m3", _e4m3_bias8, FP8_PINS),
     ("decode_e4m3", _e4m3_no_subnormals, FP8_PINS),
     ("forward_fp8", _fp8_swapped_scales, FP8_PINS),
+    ("window_visible", _window_off_by_one, WINDOW_PINS),
+    ("window_visible", _window_sides_swapped, WINDOW_PINS),
 ]
 
 
