@@ -12,6 +12,8 @@ Also measured in the same run and reported in the same JSON line:
   breakdown.decode         split-KV decode (B=64, H=32, N_kv=32768, d=128, 64 splits), GB/s
   breakdown.decode_paged   the same decode over a paged cache (256-key blocks, shuffled), GB/s
   breakdown.fwd_fp8*       forward from e4m3 Q, K, V (per-tensor scales), same shapes
+  breakdown.window         forward and forward+backward under a 4096-key causal sliding window
+                           on 1x16x16384x128
   roofline                 the dominant kernel of the step (backward main kernel), timed alone
   e2e                      the step through the public Python API with host (pinned) buffers,
                            host->device and device->host copies inside the timed region
@@ -358,6 +360,36 @@ def run_ours(args, rank, world, local_rank):
                                    "ms": round(c_ms, 4)}
     breakdown["fwd_causal"] = {"tflops": round(whole_job_rate(fl_fc, world, cf_ms * 1e-3) / 1e12, 1),
                                "ms": round(cf_ms, 4)}
+
+    # ---- sliding window on the long sequence: 1x16x16384x128, each query sees its last 4096 keys
+    wl_ = inputs.LONG
+    win = 4095
+    xw = {k_: v_.to(dev) for k_, v_ in inputs.make_workload(wl_).items()}
+    ow, lw = torch.empty_like(xw["q"]), torch.empty(xw["q"].shape[:3], dtype=torch.float32, device=dev)
+    gw = [torch.empty_like(xw["q"]) for _ in range(3)]
+    wsw = torch.empty(fa.fa_bwd_workspace_size(wl_.B, wl_.H, wl_.N_q, wl_.N_kv, wl_.d), dtype=torch.uint8,
+                      device=dev)
+    fl_wf = W.window_fwd_flops(wl_.B, wl_.H, wl_.N_q, wl_.d, win, 0)
+    fl_wb = W.window_bwd_flops(wl_.B, wl_.H, wl_.N_q, wl_.d, win, 0)
+
+    def win_fwd(pe):
+        fa.fa_fwd_window(xw["q"], xw["k"], xw["v"], ow, lw, wl_.scale, win, 0)
+
+    def win_step(pe):
+        win_fwd(pe)
+        fa.fa_bwd_window(xw["q"], xw["k"], xw["v"], ow, lw, xw["do"], gw[0], gw[1], gw[2], wsw,
+                         wl_.scale, win, 0)
+    wf_total, _ = timed(win_fwd, K)
+    ws_total, _ = timed(win_step, K)
+    wf_ms, ws_ms = reduce_max(wf_total / K), reduce_max(ws_total / K)
+    breakdown["window"] = {
+        "workload": f"{wl_.name} under a causal sliding window of {win + 1} keys (left {win}, right 0)",
+        "fwd_tflops": round(whole_job_rate(fl_wf, world, wf_ms * 1e-3) / 1e12, 1), "fwd_ms": round(wf_ms, 4),
+        "fwd_bwd_tflops": round(whole_job_rate(fl_wf + fl_wb, world, ws_ms * 1e-3) / 1e12, 1),
+        "fwd_bwd_ms": round(ws_ms, 4),
+        "flops": "4 d (fwd) and 10 d (bwd) per visible (query, key) pair",
+    }
+    del xw, ow, lw, gw, wsw
 
     # ---- FP8 forward (e4m3 Q, K, V with per-tensor scales) on the same shapes
     x8 = inputs.make_qkv_fp8(w.B, w.H, w.N_q, w.N_kv, w.d, w.seed + 7919 * rank, device=str(dev))

@@ -20,6 +20,7 @@ __all__ = [
     "fa_decode_workspace_size", "fa_sync_status", "fa_status_string", "fa_last_error_message",
     "forward", "backward", "decode", "fa_fwd_varlen", "forward_varlen",
     "fa_bwd_varlen", "backward_varlen", "fa_decode_paged", "decode_paged", "fa_fwd_fp8", "forward_fp8",
+    "fa_fwd_window", "fa_bwd_window", "forward_window", "backward_window",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -60,6 +61,8 @@ _SIGNATURES = {
     "fa_decode_workspace_size": (_S, [_I, _I, _I, _I, _I]),
     "fa_decode_splitkv": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P, _S, _P]),
     "fa_decode_splitkv_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
+    "fa_fwd_window": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "fa_bwd_window": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _F, _I, _I, _P]),
     "fa_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _F, _F, _I, _P]),
     "fa_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S,
                              _P]),
@@ -230,6 +233,22 @@ def fa_decode_splitkv_noalloc(q, k, v, o, lse, scale: float, n_splits: int, stre
                                                     _stream(stream)))
 
 
+def fa_fwd_window(q, k, v, o, lse, scale: float, window_left: int, window_right: int, stream=None):
+    B, H, N, d = q.shape
+    _check(load_library().fa_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                                        float(scale), int(window_left), int(window_right),
+                                        _stream(stream)))
+
+
+def fa_bwd_window(q, k, v, o, lse, do, dq, dk, dv, ws, scale: float, window_left: int,
+                  window_right: int, stream=None):
+    B, H, N, d = q.shape
+    _check(load_library().fa_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), _nbytes(ws), B, H,
+                                        N, d, float(scale), int(window_left), int(window_right),
+                                        _stream(stream)))
+
+
 def fa_fwd_fp8(q8, k8, v8, o, lse, scale: float, descale_q: float, descale_k: float,
                descale_v: float, causal: bool = False, stream=None):
     """q8, k8, v8: e4m3 codes (uint8 or float8_e4m3fn tensors) [B,H,N,d]; o bf16, lse fp32."""
@@ -342,3 +361,29 @@ def forward_fp8(q8, k8, v8, descale_q: float, descale_k: float, descale_v: float
     lse = torch.empty((B, H, n_q), dtype=torch.float32, device=q8.device)
     fa_fwd_fp8(q8, k8, v8, o, lse, scale, descale_q, descale_k, descale_v, causal, stream)
     return o, lse
+
+
+def forward_window(q, k, v, window_left: int, window_right: int, scale: float | None = None,
+                   stream=None):
+    """Sliding-window forward: query i sees keys i - window_left .. i + window_right (a negative
+    bound is unbounded) -> (O, lse)."""
+    import torch
+    d = q.shape[-1]
+    scale = d ** -0.5 if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    fa_fwd_window(q, k, v, o, lse, scale, window_left, window_right, stream)
+    return o, lse
+
+
+def backward_window(q, k, v, o, lse, do, window_left: int, window_right: int,
+                    scale: float | None = None, stream=None, workspace=None):
+    import torch
+    B, H, N, d = q.shape
+    scale = d ** -0.5 if scale is None else scale
+    need = fa_bwd_workspace_size(B, H, N, N, d)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_bwd_window(q, k, v, o, lse, do, dq, dk, dv, workspace, scale, window_left, window_right, stream)
+    return dq, dk, dv

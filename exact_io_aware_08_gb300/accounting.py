@@ -59,3 +59,22 @@ def fwd_bytes(B: int, H: int, n_q: int, n_kv: int, d: int) -> int:
 def bwd_bytes(B: int, H: int, n_q: int, n_kv: int, d: int) -> int:
     """Compulsory HBM bytes of the backward: read Q, K, V, O, dO, lse; write dQ, dK, dV."""
     return (3 * n_q + 2 * n_kv + 2 * n_kv + n_q) * d * 2 * B * H + 4 * n_q * B * H
+
+
+def window_pairs(n: int, left: int, right: int) -> int:
+    """Visible (query, key) pairs of one head under the window i - left <= j <= i + right over
+    n positions (a negative bound is unbounded): sum over i of the clipped window width."""
+    total = 0
+    lo_w = n if left < 0 else left
+    hi_w = n if right < 0 else right
+    for i in range(n):
+        total += min(n - 1, i + hi_w) - max(0, i - lo_w) + 1
+    return total
+
+
+def window_fwd_flops(B: int, H: int, n: int, d: int, left: int, right: int) -> int:
+    return 4 * d * window_pairs(n, left, right) * B * H
+
+
+def window_bwd_flops(B: int, H: int, n: int, d: int, left: int, right: int) -> int:
+    return 10 * d * window_pairs(n, left, right) * B * H

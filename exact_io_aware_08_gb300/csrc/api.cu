@@ -213,6 +213,44 @@ fa_status_t fa_bwd(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
   return FA_OK;
 }
 
+fa_status_t fa_fwd_window(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
+                          fa_bf16_t* o, float* lse, int B, int H, int N, int d, float scale,
+                          int window_left, int window_right, void* stream) {
+  fa_status_t st = check_shape(B, H, N, N, d, scale);
+  if (st != FA_OK) return st;
+  if (N == 0) return FA_OK;
+  if (!q || !k || !v || !o || !lse) return fail(FA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(FA_ERR_INVALID_ARG, "arrays must be 16-byte aligned");
+  fa::FwdArgs a{q, k, v, o, lse, B, H, N, N, d, scale, 0};
+  a.windowed = true;
+  a.win_left = window_left < 0 ? fa::kWinUnbounded : std::min(window_left, fa::kWinUnbounded);
+  a.win_right = window_right < 0 ? fa::kWinUnbounded : std::min(window_right, fa::kWinUnbounded);
+  cudaError_t e = fa::launch_fwd(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_window launch");
+  return FA_OK;
+}
+
+fa_status_t fa_bwd_window(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
+                          const fa_bf16_t* o, const float* lse, const fa_bf16_t* dO,
+                          fa_bf16_t* dq, fa_bf16_t* dk, fa_bf16_t* dv, void* ws, size_t ws_bytes,
+                          int B, int H, int N, int d, float scale, int window_left,
+                          int window_right, void* stream) {
+  fa::BwdArgs a;
+  const void* const ptrs[9] = {q, k, v, o, lse, dO, dq, dk, dv};
+  fa_status_t st = check_bwd(ptrs, kNeedAll, ws, ws_bytes, B, H, N, N, d, scale, 0, &a);
+  if (st != FA_OK) return st;
+  a.windowed = true;
+  a.win_left = window_left < 0 ? fa::kWinUnbounded : std::min(window_left, fa::kWinUnbounded);
+  a.win_right = window_right < 0 ? fa::kWinUnbounded : std::min(window_right, fa::kWinUnbounded);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = fa::launch_bwd_prep(a, s);
+  if (e == cudaSuccess) e = fa::launch_bwd_main(a, s);
+  if (e == cudaSuccess) e = fa::launch_bwd_finish(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_bwd_window launch");
+  return FA_OK;
+}
+
 fa_status_t fa_bwd_prep(const fa_bf16_t* o, const fa_bf16_t* dO, void* ws, size_t ws_bytes,
                         int B, int H, int N_q, int N_kv, int d, void* stream) {
   fa::BwdArgs a;

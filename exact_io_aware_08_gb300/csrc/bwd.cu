@@ -84,6 +84,8 @@ struct BwdParams {
   const int* cu_k;
   uint16_t* dk;
   uint16_t* dv;
+  // Visible keys of query i: i - win_left <= j <= i + win_right (kWinUnbounded: no bound).
+  int win_left, win_right;
 };
 
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
@@ -95,7 +97,7 @@ __device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float
                :: "l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
-template <int D, bool VL>
+template <int D, bool VL, bool WIN = false>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 bwd_main_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
@@ -141,8 +143,14 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
     if (k0 >= n_kv) return;                         // whole CTA, before any shared state
   }
   const int n_qtiles = (n_q + C::BM - 1) / C::BM;
-  const int i_start = p.causal ? (k0 / C::BM) : 0;     // first query tile that sees key k0
-  const int n = max(0, n_qtiles - i_start);
+  // Query tiles that see some key of [k0, k0 + BN): rows i with k0 - win_right <= i and
+  // i <= k0 + BN - 1 + win_left; the others are skipped (never loaded).
+  // Without a window only the causal start applies (WIN = false keeps that path lean).
+  const int wr = min(p.win_right, kWinUnbounded - C::BN);
+  const int wl = min(p.win_left, kWinUnbounded - C::BN);
+  const int i_start = WIN ? max(0, k0 - wr) / C::BM : (p.causal ? (k0 / C::BM) : 0);
+  const int i_end = WIN ? min(n_qtiles, (k0 + C::BN - 1 + wl) / C::BM + 1) : n_qtiles;
+  const int n = max(0, i_end - i_start);
   // TMA coordinates of local row ``row``: fixed length {x, row, (b,h)}; packed {x, h, beg+row}
   auto y1 = [&](int row) { return VL ? head : row; };
   auto y2 = [&](int beg, int row) { return VL ? beg + row : bh; };
@@ -322,8 +330,11 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       tc_fence_after();
       const float* s_nlse = reinterpret_cast<const float*>(stage_ptr(i % C::NST) + 2 * C::Q_TILE);
       const float* s_nd = s_nlse + C::BM;
-      const bool diag = p.causal && (q0 < k0 + C::BN - 1);
+      // a (key tile, query tile) pair that some pair of rows sees only in part
+      const bool diag = WIN ? ((q0 < k0 + C::BN - 1 - wr) || (q0 + C::BM - 1 > k0 + wl))
+                            : (p.causal && (q0 < k0 + C::BN - 1));
       const float2 c2v = make_float2(c2, c2);
+      const int c_lo = k_idx - wr - q0, c_hi = k_idx + wl - q0;
       uint32_t pk_ds[C::HALF / 2];
 #pragma unroll
       for (int c = 0; c < C::HALF / 32; ++c) {
@@ -347,8 +358,14 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
           const float2 x = ffma2(make_float2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2v,
                                  make_float2(nl[e], nl[e + 1]));
           float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-          if (row_dead || (diag && k_idx > q0 + col)) p0 = 0.f;
-          if (row_dead || (diag && k_idx > q0 + col + 1)) p1 = 0.f;
+          if constexpr (WIN) {
+            // query q0 + col sees key k_idx iff c_lo <= col <= c_hi
+            if (row_dead || (diag && (col < c_lo || col > c_hi))) p0 = 0.f;
+            if (row_dead || (diag && (col + 1 < c_lo || col + 1 > c_hi))) p1 = 0.f;
+          } else {
+            if (row_dead || (diag && k_idx > q0 + col)) p0 = 0.f;
+            if (row_dead || (diag && k_idx > q0 + col + 1)) p1 = 0.f;
+          }
           const float2 ds = fmul2(make_float2(p0, p1),
                                   fadd2(make_float2(__uint_as_float(rd[e]), __uint_as_float(rd[e + 1])),
                                         make_float2(nd[e], nd[e + 1])));
@@ -565,10 +582,18 @@ static cudaError_t launch_bwd_main_d(const BwdArgs& a, cudaStream_t stream) {
   p.cu_q = p.cu_k = nullptr;
   p.dk = static_cast<uint16_t*>(a.dk);
   p.dv = static_cast<uint16_t*>(a.dv);
+  attention_window(a.causal, a.windowed, a.win_left, a.win_right, &p.win_left, &p.win_right);
   static int attr_done[64] = {0};   // one per instantiation of this launcher
+  const uint64_t grid = static_cast<uint64_t>(p.n_kvtiles) * bh;
+  if (a.windowed) {
+    static int attr_win[64] = {0};
+    cudaError_t e = ensure_smem_attr(bwd_main_kernel<D, false, true>, C::SMEM_BYTES, attr_win);
+    if (e != cudaSuccess) return e;
+    bwd_main_kernel<D, false, true><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError();
+  }
   cudaError_t e = ensure_smem_attr(bwd_main_kernel<D, false>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
-  const uint64_t grid = static_cast<uint64_t>(p.n_kvtiles) * bh;
   bwd_main_kernel<D, false><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
@@ -607,6 +632,7 @@ static cudaError_t launch_bwd_main_varlen_d(const BwdArgs& a, cudaStream_t strea
   p.cu_k = a.cu_k;
   p.dk = static_cast<uint16_t*>(a.dk);
   p.dv = static_cast<uint16_t*>(a.dv);
+  attention_window(a.causal, false, 0, 0, &p.win_left, &p.win_right);
   static int attr_done[64] = {0};
   cudaError_t e = ensure_smem_attr(bwd_main_kernel<D, true>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;

@@ -16,6 +16,17 @@ enum DevError : unsigned int {
   FA_DEV_BAD_CONFIG = 2u,    // kernel found launch geometry it was not built for
 };
 
+// "No bound on this side" for attention windows: query i sees keys j with
+// i - win_left <= j <= i + win_right.
+constexpr int kWinUnbounded = 1 << 30;
+
+// Window of a call: an explicit window (win_left / win_right >= 0 or kWinUnbounded) when
+// ``windowed``, else causal = (unbounded, 0) or no mask = (unbounded, unbounded).
+inline void attention_window(int causal, bool windowed, int left, int right, int* wl, int* wr) {
+  *wl = windowed ? left : kWinUnbounded;
+  *wr = windowed ? right : (causal ? 0 : kWinUnbounded);
+}
+
 struct FwdArgs {
   const void* q;
   const void* k;
@@ -26,6 +37,8 @@ struct FwdArgs {
   float scale;
   int causal;
   float descale_q = 1.f, descale_k = 1.f, descale_v = 1.f;   // fp8 forward only
+  bool windowed = false;                                     // sliding window (below)
+  int win_left = kWinUnbounded, win_right = kWinUnbounded;
 };
 
 struct FwdVarlenArgs {
@@ -61,6 +74,8 @@ struct BwdArgs {
   const int* cu_q = nullptr;
   const int* cu_k = nullptr;
   int n_seqs = 0, total_q = 0, total_k = 0, max_seqlen_q = 0, max_seqlen_k = 0;
+  bool windowed = false;                                     // sliding window (as FwdArgs)
+  int win_left = kWinUnbounded, win_right = kWinUnbounded;
 };
 
 struct DecodeArgs {

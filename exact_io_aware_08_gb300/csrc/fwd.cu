@@ -92,9 +92,12 @@ struct FwdParams {
   // FP8: scale = tau * s_q * s_k (the score scale of the raw code products); O is multiplied by
   // out_scale = s_v.  bf16: out_scale = 1.
   float out_scale;
+  // Visible keys of query i: i - win_left <= j <= i + win_right (kWinUnbounded = no bound on
+  // that side).  Causal is (kWinUnbounded, 0), no mask (kWinUnbounded, kWinUnbounded).
+  int win_left, win_right;
 };
 
-template <int D, bool VL, bool F8 = false>
+template <int D, bool VL, bool F8 = false, bool WIN = false>
 __global__ void __launch_bounds__(FwdCfg<D, F8>::THREADS, 1)
 fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D, F8>;
@@ -144,14 +147,30 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
   if (r >= n_qpairs) return;                          // whole CTA, before any shared state
   const int n_kvtiles = (n_kv + C::BN - 1) / C::BN;
   const int c = p.causal ? (n_qpairs - 1 - r) : r;
-  int q0[2], n_t[2];
+  // Key tiles of query tile t: [lo_t, lo_t + n_t[t]) -- every tile holding a key that some row
+  // of the tile sees; tiles entirely outside every row's window are skipped, never loaded
+  // ("Causal masks": the same skipping serves sliding windows).  The CTA streams the union
+  // [j0, j0 + n_max) once (the two ranges overlap: both tiles see their diagonals), so tile t
+  // starts at position off[t] of that stream.
+  int q0[2], n_t[2], off[2], lo[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     q0[t] = c * 2 * C::BM + t * C::BM;
-    const int tile_index = 2 * c + t;                 // in units of 128 rows
-    n_t[t] = (q0[t] >= n_q) ? 0 : (p.causal ? min(tile_index + 1, n_kvtiles) : n_kvtiles);
+    if constexpr (WIN) {
+      const int first_key = max(0, q0[t] - p.win_left);
+      const int last_key = min(n_kv - 1, q0[t] + C::BM - 1 + min(p.win_right, kWinUnbounded - C::BM));
+      lo[t] = first_key / C::BN;
+      const int hi = (last_key < first_key) ? lo[t] : min(n_kvtiles, last_key / C::BN + 1);
+      n_t[t] = (q0[t] >= n_q) ? 0 : hi - lo[t];
+    } else {                                          // causal or no mask: from key tile 0
+      lo[t] = 0;
+      n_t[t] = (q0[t] >= n_q) ? 0 : (p.causal ? min(2 * c + t + 1, n_kvtiles) : n_kvtiles);
+    }
   }
-  const int n_max = max(n_t[0], n_t[1]);
+  const int j0 = WIN ? lo[0] : 0;
+  const int n_max = WIN ? ((n_t[1] > 0) ? lo[1] + n_t[1] - j0 : n_t[0]) : max(n_t[0], n_t[1]);
+  off[0] = 0;
+  off[1] = lo[1] - j0;
   // TMA coordinates of local row ``row``: fixed length {x, row, (b,h)}; packed {x, h, beg+row}
   auto y1 = [&](int row) { return VL ? head : row; };
   auto y2 = [&](int beg, int row) { return VL ? beg + row : bh; };
@@ -193,17 +212,18 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       for (int t = 0; t < nq_tiles; ++t)
         for (int k = 0; k < C::KCH; ++k)
           tma_load_3d(sQ + t * C::TILE + k * C::CHUNK, &p.tq, q_full, k * C::XCH, y1(q0[t]), y2(q_beg, q0[t]));
-      for (int j = 0; j < n_max; ++j) {
+      for (int j = 0; j < n_max; ++j) {               // stream position j = key tile j0 + j
         const int s = j % C::NS;
         const uint32_t u = j / C::NS;
+        const int key = (j0 + j) * C::BN;
         if (u > 0 && !mbar_wait(&k_empty[s], (u - 1) & 1, abort_flag, 101)) break;
         mbar_arrive_expect_tx(&k_full[s], C::TILE);
         for (int k = 0; k < C::KCH; ++k)
-          tma_load_3d(sK + s * C::TILE + k * C::CHUNK, &p.tk, &k_full[s], k * C::XCH, y1(j * C::BN), y2(k_beg, j * C::BN));
+          tma_load_3d(sK + s * C::TILE + k * C::CHUNK, &p.tk, &k_full[s], k * C::XCH, y1(key), y2(k_beg, key));
         if (u > 0 && !mbar_wait(&v_empty[s], (u - 1) & 1, abort_flag, 102)) break;
         mbar_arrive_expect_tx(&v_full[s], C::TILE);
         for (int k = 0; k < C::KCH; ++k)
-          tma_load_3d(sV + s * C::TILE + k * C::CHUNK, &p.tv, &v_full[s], k * C::XCH, y1(j * C::BN), y2(k_beg, j * C::BN));
+          tma_load_3d(sV + s * C::TILE + k * C::CHUNK, &p.tv, &v_full[s], k * C::XCH, y1(key), y2(k_beg, key));
         issued = j + 1;
       }
       if (*abort_flag) {
@@ -239,7 +259,7 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
         }
         umma_commit(&s_full[t]);
       };
-      auto issue_pv = [&](int t, int j) {                       // O_t += P_t V_j
+      auto issue_pv = [&](int t, int j, bool first) {           // O_t += P_t V_j
         const uint64_t b = desc_advance(dv0, (j % C::NS) * C::TILE);
         const uint32_t d_tmem = tbase + C::T_O + t * D;
         const uint32_t a_tmem = tbase + C::T_S + t * 128;
@@ -247,32 +267,34 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
         for (int ks = 0; ks < C::KS_PV; ++ks) {
           if constexpr (F8)
             umma_ts_f8(d_tmem, a_tmem + ks * 8, desc_advance(b, ks * C::PV_B_STEP), idesc_o,
-                       (j > 0 || ks > 0) ? 1u : 0u);
+                       (!first || ks > 0) ? 1u : 0u);
           else
             umma_ts(d_tmem, a_tmem + ks * 8, desc_advance(b, ks * C::PV_B_STEP), idesc_o,
-                    (j > 0 || ks > 0) ? 1u : 0u);
+                    (!first || ks > 0) ? 1u : 0u);
         }
       };
       bool ok = mbar_wait(q_full, 0, abort_flag, 111) && mbar_wait(&k_full[0], 0, abort_flag, 112);
       if (ok) {
         tc_fence_after();
         if (n_t[0] > 0) issue_s(0, 0);
-        if (n_t[1] > 0) issue_s(1, 0);
+        if (n_t[1] > 0 && (!WIN || off[1] == 0)) issue_s(1, 0);
         umma_commit(&k_empty[0]);
       }
+      // stream position j; tile t is on its i-th key tile, i = j - off[t]
       for (int j = 0; ok && j < n_max; ++j) {
         const int s = j % C::NS;
         if (!(ok = mbar_wait(&v_full[s], (j / C::NS) & 1, abort_flag, 113))) break;
         bool k_ready = false;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          if (j < n_t[t]) {
-            if (!(ok = mbar_wait(&p_full[t], j & 1, abort_flag, 115 + t))) break;
+          const int i = WIN ? j - off[t] : j;       // without a window both tiles start at 0
+          if ((!WIN || i >= 0) && i < n_t[t]) {
+            if (!(ok = mbar_wait(&p_full[t], i & 1, abort_flag, 115 + t))) break;
             tc_fence_after();
-            issue_pv(t, j);
-            if (j + 1 == n_t[t]) umma_commit(&o_done[t]);
+            issue_pv(t, j, i == 0);
+            if (i + 1 == n_t[t]) umma_commit(&o_done[t]);
           }
-          if (j + 1 < n_t[t]) {
+          if ((!WIN || i + 1 >= 0) && i + 1 < n_t[t]) {
             if (!k_ready) {
               if (!(ok = mbar_wait(&k_full[(j + 1) % C::NS], ((j + 1) / C::NS) & 1, abort_flag, 114)))
                 break;
@@ -298,8 +320,13 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
     const uint32_t t_lane = static_cast<uint32_t>(sub * 32) << 16;
     const uint32_t t_s = tbase + t_lane + C::T_S + t * 128;
     const uint32_t t_o = tbase + t_lane + C::T_O + t * D;
-    const int q_idx = q0[t] + row;
+    const int q0t = q0[t];                    // this warpgroup's tile, hoisted out of the arrays
+    const int lo_t = WIN ? lo[t] : 0;
+    const int q_idx = q0t + row;
     const int n = n_t[t];
+    // this row's visible keys [key_lo, key_hi) under a window
+    const int key_lo = WIN ? max(0, q_idx - p.win_left) : 0;
+    const int key_hi = WIN ? min(n_kv, q_idx + 1 + min(p.win_right, kWinUnbounded - C::BM)) : 0;
     const float c2 = p.scale_log2;
     float m = -INFINITY;                      // reference max (raw dot-product units)
     float l = 0.f;                            // sum of 2^{(s - m) c2} over keys seen (fp32)
@@ -319,8 +346,17 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       }
       tmem_wait_ld();
 
-      const int k0 = j * C::BN;
-      if (k0 + C::BN > n_kv || (p.causal && k0 + C::BN - 1 > q0[t])) {
+      const int k0 = (lo_t + j) * C::BN;
+      // a tile that some row of the query tile sees only in part (window edge, causal
+      // diagonal, ragged end of the keys) is masked element by element
+      if constexpr (WIN) {
+        if (k0 + C::BN > n_kv || k0 + C::BN - 1 > q0t + min(p.win_right, kWinUnbounded - C::BM) ||
+            k0 < q0t + C::BM - 1 - p.win_left) {
+#pragma unroll
+          for (int k = 0; k < 128; ++k)
+            if (k0 + k < key_lo || k0 + k >= key_hi) s[k] = -INFINITY;
+        }
+      } else if (k0 + C::BN > n_kv || (p.causal && k0 + C::BN - 1 > q0t)) {
         const int lim = p.causal ? min(q_idx + 1, n_kv) : n_kv;   // keys < lim visible
 #pragma unroll
         for (int k = 0; k < 128; ++k)
@@ -337,7 +373,10 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       }
       const float mx = fmaxf(fmax3(mq[0], mq[1], mq[2]), mq[3]);
       const float cand = fmaxf(m, mx);
-      const bool move = (m == -INFINITY) || ((cand - m) * c2 > C::RESCALE_THRESHOLD);
+      // (under a window a row may miss a whole tile: cand = -inf, nothing to move; without
+      // one every row sees a key of its first tile)
+      const bool move = (!WIN || cand != -INFINITY) &&
+                        ((m == -INFINITY) || ((cand - m) * c2 > C::RESCALE_THRESHOLD));
       if (__any_sync(0xffffffffu, move)) {
         const float alpha = move ? fast_exp2((m - cand) * c2) : 1.f;  // 0 when m = -inf
         if (move) {
@@ -501,10 +540,18 @@ static cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   p.cu_q = p.cu_k = nullptr;
   p.o = static_cast<uint16_t*>(a.o);
   p.out_scale = 1.f;
+  attention_window(a.causal, a.windowed, a.win_left, a.win_right, &p.win_left, &p.win_right);
   static int attr_done[64] = {0};   // one per instantiation of this launcher
+  const uint64_t grid = static_cast<uint64_t>(p.n_qpairs) * bh;
+  if (a.windowed) {
+    static int attr_win[64] = {0};
+    cudaError_t e = ensure_smem_attr(fwd_kernel<D, false, false, true>, C::SMEM_BYTES, attr_win);
+    if (e != cudaSuccess) return e;
+    fwd_kernel<D, false, false, true><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError();
+  }
   cudaError_t e = ensure_smem_attr(fwd_kernel<D, false>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
-  const uint64_t grid = static_cast<uint64_t>(p.n_qpairs) * bh;
   fwd_kernel<D, false><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
@@ -536,6 +583,7 @@ static cudaError_t launch_fwd_varlen_d(const FwdVarlenArgs& a, cudaStream_t stre
   p.cu_k = a.cu_k;
   p.o = static_cast<uint16_t*>(a.o);
   p.out_scale = 1.f;
+  attention_window(a.causal, false, 0, 0, &p.win_left, &p.win_right);
   static int attr_done[64] = {0};
   cudaError_t e = ensure_smem_attr(fwd_kernel<D, true>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
@@ -571,6 +619,7 @@ cudaError_t launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream) {
   p.cu_q = p.cu_k = nullptr;
   p.o = static_cast<uint16_t*>(a.o);
   p.out_scale = a.descale_v;
+  attention_window(a.causal, false, 0, 0, &p.win_left, &p.win_right);
   static int attr_done[64] = {0};
   cudaError_t e = ensure_smem_attr(fwd_kernel<D, false, true>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;

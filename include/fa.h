@@ -65,6 +65,26 @@ fa_status_t fa_fwd(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v, f
                    void* stream);
 
 /*
+ * fa_fwd_window / fa_bwd_window -- attention under a sliding window, forward and backward
+ * ([Lesson4] section 6 "Where it shows up": long-context training uses causal and
+ * sliding-window masks, both with tile skipping; section "Causal masks" for the skipping).
+ *
+ * Query i sees key j iff  i - window_left <= j <= i + window_right  over one sequence
+ * (N_q = N_kv = N); a negative bound is unbounded on that side, so (-1, 0) is causal and
+ * (-1, -1) is no mask.  Key tiles outside every row of a query tile's windows are never
+ * loaded; tiles cut by a window edge are masked element by element.  Otherwise exactly
+ * fa_fwd / fa_bwd (same layouts, workspace, errors).
+ */
+fa_status_t fa_fwd_window(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
+                          fa_bf16_t* o, float* lse, int B, int H, int N, int d, float scale,
+                          int window_left, int window_right, void* stream);
+fa_status_t fa_bwd_window(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
+                          const fa_bf16_t* o, const float* lse, const fa_bf16_t* dO,
+                          fa_bf16_t* dq, fa_bf16_t* dk, fa_bf16_t* dv, void* ws, size_t ws_bytes,
+                          int B, int H, int N, int d, float scale, int window_left,
+                          int window_right, void* stream);
+
+/*
  * fa_fwd_fp8 -- attention forward from 8-bit inputs (the low-precision FP8 path [Lesson4]
  * "Causal masks and FlashAttention-3" and [Scratch] "Later versions" name; the pages give no
  * formula, so this follows the plainest reading: one scale per tensor).

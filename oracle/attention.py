@@ -422,3 +422,19 @@ def backward_window(q, k, v, do, scale: float, left: int, right: int):
             dq[b, h] = scale * (ds @ k[b, h])
             dk[b, h] = scale * (ds.T @ q[b, h])
     return dq, dk, dv
+
+
+def forward_window_rows(q_rows, row_index, k, v, scale: float, left: int, right: int):
+    """Sliding-window forward for selected query rows of one head (full-size sampling); the
+    same definition as ``forward_window_head`` evaluated for a subset of independent rows."""
+    q_rows, k, v = _as_f64(q_rows), _as_f64(k), _as_f64(v)
+    s = scale * (q_rows @ k.T)
+    i = np.asarray(row_index)[:, None]
+    j = np.arange(k.shape[0])[None, :]
+    vis = np.ones(s.shape, dtype=bool)
+    if left >= 0:
+        vis &= j >= i - left
+    if right >= 0:
+        vis &= j <= i + right
+    p, m, l = three_pass_softmax(np.where(vis, s, NEG_INF))
+    return p @ v, lse_from(m, l)

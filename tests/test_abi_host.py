@@ -153,3 +153,14 @@ def test_fwd_fp8_rejection(lib):
     assert call(dq=1e-30, dk=1e-30) == INVALID          # the product underflows to 0
     assert call(causal=1, N_kv=128) == UNSUPPORTED
     assert call(k=FAKE + 8) == INVALID
+
+
+def test_window_entry_points_validate_like_the_plain_ones(lib):
+    st = lib.fa_fwd_window(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 256, 96, 0.1, 10, 0, None)
+    assert st == UNSUPPORTED
+    st = lib.fa_fwd_window(FAKE, None, FAKE, FAKE, FAKE, 1, 2, 256, 128, 0.1, 10, 0, None)
+    assert st == INVALID
+    need = lib.fa_bwd_workspace_size(1, 2, 256, 256, 128)
+    args = [FAKE] * 9
+    st = lib.fa_bwd_window(*args, FAKE, need - 1, 1, 2, 256, 128, 0.1, 10, 0, None)
+    assert st == WORKSPACE

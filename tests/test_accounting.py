@@ -28,3 +28,19 @@ def test_pairs_and_flop_ratios():
     assert W.pairs(3, 5, False) == 15
     # the backward is 25% more matmul work than the four plain matmuls (10 vs 8 N^2 d)
     assert W.bwd_flops(1, 1, 64, 64, 32, False) * 8 == W.fwd_flops(1, 1, 64, 64, 32, False) * 20
+
+
+def test_window_pairs_special_cases_and_brute_force():
+    import numpy as np
+    assert W.window_pairs(100, -1, 0) == W.pairs(100, 100, True)
+    assert W.window_pairs(100, -1, -1) == W.pairs(100, 100, False)
+    assert W.window_pairs(100, 0, 0) == 100
+    for n, l, r in ((37, 5, 0), (37, 3, 9), (10, 20, 2), (64, -1, 7)):
+        i = np.arange(n)[:, None]
+        j = np.arange(n)[None, :]
+        vis = np.ones((n, n), dtype=bool)
+        if l >= 0:
+            vis &= j >= i - l
+        if r >= 0:
+            vis &= j <= i + r
+        assert W.window_pairs(n, l, r) == int(vis.sum())

@@ -490,3 +490,13 @@ def test_window_backward_vs_torch_autograd(left, right):
     np.testing.assert_allclose(dq, qt.grad.numpy(), atol=1e-12)
     np.testing.assert_allclose(dk, kt.grad.numpy(), atol=1e-12)
     np.testing.assert_allclose(dv, vt.grad.numpy(), atol=1e-12)
+
+
+def test_window_rows_match_full_head():
+    q, k, v, _ = _qkv(5, N=50)
+    rows = np.array([0, 3, 17, 49])
+    for left, right in ((4, 0), (7, 3), (-1, 2)):
+        o, lse, _ = A.forward_window_head(q[0, 1], k[0, 1], v[0, 1], 0.3, left, right)
+        o_r, lse_r = A.forward_window_rows(q[0, 1, rows], rows, k[0, 1], v[0, 1], 0.3, left, right)
+        np.testing.assert_allclose(o_r, o[rows], atol=1e-14)
+        np.testing.assert_allclose(lse_r, lse[rows], atol=1e-14)
