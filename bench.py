@@ -427,21 +427,74 @@ def run_ours(args, rank, world, local_rank):
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in out_host.values())
 
-    def e2e_step(pe):
-        q = host["q"].to(dev, non_blocking=True)
-        k_ = host["k"].to(dev, non_blocking=True)
-        v = host["v"].to(dev, non_blocking=True)
-        do = host["do"].to(dev, non_blocking=True)
-        o, lse = fa.forward(q, k_, v, causal=w.causal, scale=w.scale)
-        dq, dk, dv = fa.backward(q, k_, v, o, lse, do, causal=w.causal, scale=w.scale,
-                                 workspace=d["ws"])
-        for name, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
-            out_host[name].copy_(t, non_blocking=True)
-    e_total, _ = timed(e2e_step, K)
-    e_ms = reduce_max(e_total / K)
+    # Pipelined like a training input loop: step i+1's inputs go host->device on one copy stream
+    # while step i computes, and step i's outputs go device->host on another (o and lse as soon
+    # as the forward ends, the gradients after the backward).  Inputs and outputs are double
+    # buffered on the device; every step's copies fall inside the timed region.
+    cs = stream
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    dbuf = [{k_: torch.empty_like(d[k_]) for k_ in ("q", "k", "v", "do")} for _ in range(2)]
+    dout = [{"o": torch.empty_like(d["q"]), "lse": torch.empty_like(d["lse"]), "dq": torch.empty_like(d["q"]),
+             "dk": torch.empty_like(d["k"]), "dv": torch.empty_like(d["v"])} for _ in range(2)]
+    in_ready = [torch.cuda.Event() for _ in range(2)]
+    in_free = [torch.cuda.Event() for _ in range(2)]
+    fwd_done = [torch.cuda.Event() for _ in range(2)]
+    bwd_done = [torch.cuda.Event() for _ in range(2)]
+    out_free = [torch.cuda.Event() for _ in range(2)]
+
+    def issue_h2d(i):
+        sl = i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(in_free[sl])
+            for k_ in ("q", "k", "v", "do"):
+                dbuf[sl][k_].copy_(host[k_], non_blocking=True)
+            in_ready[sl].record(s_in)
+
+    def e2e_run(n_steps):
+        issue_h2d(0)
+        for i in range(n_steps):
+            sl = i % 2
+            if i + 1 < n_steps:
+                issue_h2d(i + 1)
+            b, o = dbuf[sl], dout[sl]
+            cs.wait_event(in_ready[sl])
+            if i >= 2:
+                cs.wait_event(out_free[sl])
+            fa.fa_fwd(b["q"], b["k"], b["v"], o["o"], o["lse"], w.scale, w.causal, cs)
+            fwd_done[sl].record(cs)
+            fa.fa_bwd(b["q"], b["k"], b["v"], o["o"], o["lse"], b["do"], o["dq"], o["dk"], o["dv"], d["ws"],
+                      w.scale, w.causal, cs)
+            in_free[sl].record(cs)
+            bwd_done[sl].record(cs)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(fwd_done[sl])
+                out_host["o"].copy_(o["o"], non_blocking=True)
+                out_host["lse"].copy_(o["lse"], non_blocking=True)
+                s_out.wait_event(bwd_done[sl])
+                for k_ in ("dq", "dk", "dv"):
+                    out_host[k_].copy_(o[k_], non_blocking=True)
+                out_free[sl].record(s_out)
+        cs.wait_stream(s_out)
+        cs.wait_stream(s_in)
+
+    e2e_run(Wm)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    es, ee = ev(), ev()
+    es.record(cs)
+    e2e_run(K)
+    ee.record(cs)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    e_ms = reduce_max(es.elapsed_time(ee) / K)
     e2e = {"value": round(whole_job_rate(fl_f + fl_b, world, e_ms * 1e-3) / 1e12, 1), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 4),
-           "api": "exact_io_aware_08_gb300.forward/backward (C ABI fa_fwd/fa_bwd)"}
+           "api": "exact_io_aware_08_gb300.fa_fwd / fa_bwd (C ABI), pinned host buffers, copies on two "
+                  "streams overlapped with the previous / next step's compute"}
+    del dbuf, dout
     del d, x, host, out_host
     torch.cuda.empty_cache()
 
