@@ -53,9 +53,9 @@ struct BwdCfg {
   static constexpr int OFF_ST = 2 * KV_TILE;
   static constexpr int OFF_DS = OFF_ST + NST * STAGE;
   static constexpr int OFF_BAR = OFF_DS + DS_TILE;
-  // kv_full, stage_full[NST], stage_empty[NST], st_full, pds_ready, pds_free,
+  // kv_full, stage_full[NST], stage_empty[NST], st_full, p_ready, ds_ready, pds_free,
   // dq_full[2], dq_free[2], mma_done
-  static constexpr int NBAR = 1 + 2 * NST + 8;
+  static constexpr int NBAR = 1 + 2 * NST + 9;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -111,8 +111,9 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
   uint64_t* stage_full = bars + 1;
   uint64_t* stage_empty = stage_full + C::NST;
   uint64_t* st_full = stage_empty + C::NST;
-  uint64_t* pds_ready = st_full + 1;
-  uint64_t* pds_free = pds_ready + 1;
+  uint64_t* p_ready = st_full + 1;       // P^T of the step is in TMEM (dV may start)
+  uint64_t* ds_ready = p_ready + 1;      // dS^T of the step is in shared memory (dK, dQ may start)
+  uint64_t* pds_free = ds_ready + 1;
   uint64_t* dq_full = pds_free + 1;      // [2], one per dQ TMEM buffer
   uint64_t* dq_free = dq_full + 2;       // [2]
   uint64_t* mma_done = dq_free + 2;
@@ -168,7 +169,8 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       mbar_init(&stage_empty[s], 1);
     }
     mbar_init(st_full, 1);
-    mbar_init(pds_ready, C::DS_THREADS);
+    mbar_init(p_ready, C::DS_THREADS);
+    mbar_init(ds_ready, C::DS_THREADS);
     mbar_init(pds_free, 1);
     for (int b2 = 0; b2 < 2; ++b2) {
       mbar_init(&dq_full[b2], 1);
@@ -266,11 +268,14 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
         tc_fence_after();
         issue_s_dp(0);
       }
-      // Per step i: dV_i (P^T from TMEM, over the S^T columns), then S/dP of step i+1 (they
-      // overwrite those columns, so they come after dV_i in issue order), then dK_i and dQ_i.
+      // Per step i: dV_i as soon as P^T_i is in TMEM (over the S^T columns), then S/dP of step
+      // i+1 (they overwrite those columns, so they come after dV_i in issue order; the dS warps
+      // have read S^T_i and dP^T_i before signalling P^T), then dK_i and dQ_i once dS^T_i is in
+      // shared memory.  The tensor core thus runs dV_i and S/dP_{i+1} while the dS warps still
+      // form dS_i, and dK_i/dQ_i while they start on step i+1.
       for (int i = 0; ok && i < n; ++i) {
         const int s = i % C::NST;
-        if (!(ok = mbar_wait(pds_ready, i & 1, abort_flag, 215))) break;
+        if (!(ok = mbar_wait(p_ready, i & 1, abort_flag, 215))) break;
         tc_fence_after();
         const uint64_t q_mn = desc_advance(dST_mn, s * C::STAGE);
         const uint64_t do_mn = desc_advance(dST_mn, s * C::STAGE + C::Q_TILE);
@@ -284,6 +289,8 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
           tc_fence_after();
           issue_s_dp(i + 1);
         }
+        if (!(ok = mbar_wait(ds_ready, i & 1, abort_flag, 218))) break;
+        tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < C::BM / 16; ++ks) {     // dK += dS^T Q
           const uint32_t a_off = (ks >> 2) * C::KV_CHUNK + (ks & 3) * 32;
@@ -336,19 +343,26 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       const float2 c2v = make_float2(c2, c2);
       const int c_lo = k_idx - wr - q0, c_hi = k_idx + wl - q0;
       uint32_t pk_ds[C::HALF / 2];
+      // P (exp) first; P^T goes back over S^T columns this thread has already read (its own
+      // half, bf16 pairs): group g's query q sits at column g*HALF + (q - g*HALF)/2, where the
+      // dV product reads it.  p_ready is signalled as soon as every thread has stored its P^T
+      // and read its dP^T, so dV and the next S/dP products (which overwrite S^T and dP^T)
+      // overlap the dS math below.
+      float pf[C::HALF], dpf[C::HALF], ndf[C::HALF];
 #pragma unroll
       for (int c = 0; c < C::HALF / 32; ++c) {
         uint32_t rs[32], rd[32];
         tmem_ld32(tbase + t_lane + C::T_S + cb + c * 32, rs);
         tmem_ld32(tbase + t_lane + C::T_DP + cb + c * 32, rd);
         // per-column -lse (log2 units) and -D: the same for every thread (broadcast reads)
-        float nl[32], nd[32];
+        float nl[32];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           const float4 a = *reinterpret_cast<const float4*>(s_nlse + cb + c * 32 + e);
           const float4 b4 = *reinterpret_cast<const float4*>(s_nd + cb + c * 32 + e);
           nl[e] = a.x; nl[e + 1] = a.y; nl[e + 2] = a.z; nl[e + 3] = a.w;
-          nd[e] = b4.x; nd[e + 1] = b4.y; nd[e + 2] = b4.z; nd[e + 3] = b4.w;
+          ndf[c * 32 + e] = b4.x; ndf[c * 32 + e + 1] = b4.y;
+          ndf[c * 32 + e + 2] = b4.z; ndf[c * 32 + e + 3] = b4.w;
         }
         tmem_wait_ld();
         uint32_t pk_p[16];
@@ -366,15 +380,23 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
             if (row_dead || (diag && k_idx > q0 + col)) p0 = 0.f;
             if (row_dead || (diag && k_idx > q0 + col + 1)) p1 = 0.f;
           }
-          const float2 ds = fmul2(make_float2(p0, p1),
-                                  fadd2(make_float2(__uint_as_float(rd[e]), __uint_as_float(rd[e + 1])),
-                                        make_float2(nd[e], nd[e + 1])));
+          pf[c * 32 + e] = p0;
+          pf[c * 32 + e + 1] = p1;
+          dpf[c * 32 + e] = __uint_as_float(rd[e]);
+          dpf[c * 32 + e + 1] = __uint_as_float(rd[e + 1]);
           pk_p[e / 2] = pack_bf16x2(p0, p1);
-          pk_ds[c * 16 + e / 2] = pack_bf16x2(ds.x, ds.y);
         }
-        // P^T goes back over S^T columns this thread has already read (its own half, bf16 pairs):
-        // group g's query q sits at column g*HALF + (q - g*HALF)/2, where the dV product reads it
         tmem_st16(tbase + t_lane + C::T_S + cb + c * 16, pk_p);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_ready);
+      // dS^T = P^T o (dP^T - D)
+#pragma unroll
+      for (int e = 0; e < C::HALF; e += 2) {
+        const float2 ds = fmul2(make_float2(pf[e], pf[e + 1]),
+                                fadd2(make_float2(dpf[e], dpf[e + 1]), make_float2(ndf[e], ndf[e + 1])));
+        pk_ds[e / 2] = pack_bf16x2(ds.x, ds.y);
       }
       if (i > 0 && !(ok = mbar_wait_warp(pds_free, (i - 1) & 1, abort_flag, 222))) break;
 #pragma unroll
@@ -384,10 +406,8 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
         *reinterpret_cast<uint4*>(sDS + off) =
             make_uint4(pk_ds[4 * u], pk_ds[4 * u + 1], pk_ds[4 * u + 2], pk_ds[4 * u + 3]);
       }
-      tmem_wait_st();
-      tc_fence_before();
       fence_proxy_async_smem();
-      mbar_arrive(pds_ready);
+      mbar_arrive(ds_ready);
     }
     // ---------------------------------------------------------------- epilogue: dK, dV
     if (ok && n > 0) {
