@@ -52,10 +52,13 @@ struct BwdCfg {
   static constexpr int OFF_V = KV_TILE;
   static constexpr int OFF_ST = 2 * KV_TILE;
   static constexpr int OFF_DS = OFF_ST + NST * STAGE;
-  static constexpr int OFF_BAR = OFF_DS + DS_TILE;
+  // d = 128: staging of one fp32 dQ tile [BM queries][d] for the TMA reduce-add into dQ_acc
+  static constexpr int DQS_BYTES = (D == 128) ? BM * D * 4 : 0;
+  static constexpr int OFF_DQS = OFF_DS + DS_TILE;
+  static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
   // kv_full, stage_full[NST], stage_empty[NST], st_full, p_ready, ds_ready, pds_free,
-  // dq_full[2], dq_free[2], mma_done
-  static constexpr int NBAR = 1 + 2 * NST + 9;
+  // dq_full[2], dq_free[2], mma_done, dqs_sync
+  static constexpr int NBAR = 1 + 2 * NST + 10;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -72,6 +75,7 @@ struct BwdCfg {
 
 struct BwdParams {
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
+  CUtensorMap tdq;                                  // fp32 dQ accumulator (d = 128)
   const float* lse;
   const float* delta;
   float* dq_acc;
@@ -117,6 +121,7 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
   uint64_t* dq_full = pds_free + 1;      // [2], one per dQ TMEM buffer
   uint64_t* dq_free = dq_full + 2;       // [2]
   uint64_t* mma_done = dq_free + 2;
+  uint64_t* dqs_sync = mma_done + 1;     // the four dQ warps around the staging buffer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -177,6 +182,7 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       mbar_init(&dq_free[b2], 128);
     }
     mbar_init(mma_done, 1);
+    mbar_init(dqs_sync, 4);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -468,24 +474,52 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
     const int sub = warp & 3;
     const int rr_ = sub * 32 + lane;               // TMEM lane: d (d=128) or query (d=64)
     const uint32_t t_lane = static_cast<uint32_t>(sub * 32) << 16;
-    for (int i = 0; i < n; ++i) {
-      const int q0 = (i_start + i) * C::BM;
-      const int qb = i & 1;
-      if (!mbar_wait_warp(&dq_full[qb], (i >> 1) & 1, abort_flag, 231)) break;
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tbase + t_lane + C::T_DQ + qb * 64 + c * 32, v);
+    if constexpr (D == 128) {
+      // lane = d, columns = queries.  Each step's tile goes TMEM -> registers (the TMEM buffer
+      // is released at once) -> a row-major [BM][d] fp32 box in shared memory -> one TMA
+      // reduce-add into dQ_acc, issued by one thread; the L2 performs the fp32 adds.
+      float* stg = reinterpret_cast<float*>(smem + C::OFF_DQS);
+      const bool leader = threadIdx.x == 320;
+      uint32_t use = 0;                              // dqs_sync phases used so far
+      for (int i = 0; i < n; ++i) {
+        const int q0 = (i_start + i) * C::BM;
+        const int qb = i & 1;
+        if (!mbar_wait_warp(&dq_full[qb], (i >> 1) & 1, abort_flag, 231)) break;
+        tc_fence_after();
+        uint32_t v[2][32];
+        tmem_ld32(tbase + t_lane + C::T_DQ + qb * 64, v[0]);
+        tmem_ld32(tbase + t_lane + C::T_DQ + qb * 64 + 32, v[1]);
         tmem_wait_ld();
-        if constexpr (D == 128) {
-          // lane = d, columns = queries q0 + c*32 + e
-          float* base = p.dq_acc + qrow(q0 + c * 32) * D + rr_;
-          const size_t step = VL ? static_cast<size_t>(p.heads) * D : static_cast<size_t>(D);
+        tc_fence_before();
+        mbar_arrive(&dq_free[qb]);
+        // the previous reduce must have finished reading the staging box
+        if (leader && i > 0) bulk_wait_group_read0();
+        if (!warps_sync(dqs_sync, use++ & 1, abort_flag, 232)) break;
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (q0 + c * 32 + e < n_q) red_add_f32(base + e * step, __uint_as_float(v[e]));
-        } else {
+        for (int c = 0; c < 2; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e) stg[(c * 32 + e) * D + rr_] = __uint_as_float(v[c][e]);
+        fence_proxy_async_smem();
+        if (!warps_sync(dqs_sync, use++ & 1, abort_flag, 233)) break;
+        // rows past the sequence's end hold zeros (their P, hence dS, is 0): adding them to
+        // whatever follows is harmless, and rows past the tensor are clipped
+        if (leader) {
+          tma_reduce_add_3d(&p.tdq, stg, 0, VL ? head : q0, VL ? q_beg + q0 : bh);
+          bulk_commit_group();
+        }
+      }
+      if (leader) bulk_wait_group0();
+    } else {
+      for (int i = 0; i < n; ++i) {
+        const int q0 = (i_start + i) * C::BM;
+        const int qb = i & 1;
+        if (!mbar_wait_warp(&dq_full[qb], (i >> 1) & 1, abort_flag, 231)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tbase + t_lane + C::T_DQ + qb * 64 + c * 32, v);
+          tmem_wait_ld();
           // lane = query q0 + rr_, columns = d
           if (q0 + rr_ < n_q) {
             float* base = p.dq_acc + qrow(q0 + rr_) * D + c * 32;
@@ -495,9 +529,9 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
                              __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
           }
         }
+        tc_fence_before();
+        mbar_arrive(&dq_free[qb]);
       }
-      tc_fence_before();
-      mbar_arrive(&dq_free[qb]);
     }
   }
 
@@ -580,7 +614,8 @@ static cudaError_t launch_bwd_main_d(const BwdArgs& a, cudaStream_t stream) {
   const uint64_t nq = a.n_q > 0 ? a.n_q : 1;
   const void* qb = a.n_q > 0 ? a.q : a.k;
   const void* dob = a.n_q > 0 ? a.dO : a.k;
-  if (!make_map_bf16_3d(&p.tq, qb, D, nq, bh, 64, C::BM) ||
+  if ((D == 128 && !make_map_f32_3d(&p.tdq, a.dq_acc, D, nq, bh, D * 4, D * 4 * nq, D, C::BM, 1)) ||
+      !make_map_bf16_3d(&p.tq, qb, D, nq, bh, 64, C::BM) ||
       !make_map_bf16_3d(&p.tdo, dob, D, nq, bh, 64, C::BM) ||
       !make_map_bf16_3d(&p.tk, a.k, D, a.n_kv, bh, 64, C::BN) ||
       !make_map_bf16_3d(&p.tv, a.v, D, a.n_kv, bh, 64, C::BN) ||
@@ -627,7 +662,9 @@ static cudaError_t launch_bwd_main_varlen_d(const BwdArgs& a, cudaStream_t strea
   const int tq = a.total_q > 0 ? a.total_q : 1;
   const void* qb = a.total_q > 0 ? a.q : a.k;
   const void* dob = a.total_q > 0 ? a.dO : a.k;
-  if (!make_map_bf16_tok(&p.tq, qb, D, a.H, tq, 64, C::BM) ||
+  if ((D == 128 && !make_map_f32_3d(&p.tdq, a.dq_acc, D, a.H, tq, D * 4, static_cast<uint64_t>(D) * 4 * a.H,
+                                    D, 1, C::BM)) ||
+      !make_map_bf16_tok(&p.tq, qb, D, a.H, tq, 64, C::BM) ||
       !make_map_bf16_tok(&p.tdo, dob, D, a.H, tq, 64, C::BM) ||
       !make_map_bf16_tok(&p.tk, a.k, D, a.H, a.total_k, 64, C::BN) ||
       !make_map_bf16_tok(&p.tv, a.v, D, a.H, a.total_k, 64, C::BN) ||
