@@ -625,7 +625,31 @@ def run_profile_case(args):
     fa.load_library()
     B, H, N, d = (int(v) for v in args.shape.split(","))
     scale = d ** -0.5
-    if args.profile == "decode":
+    if args.profile == "fwd8":
+        x = inputs.make_qkv_fp8(B, H, N, N, d, 4242, device="cuda")
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+        op = lambda: fa.fa_fwd_fp8(x["q8"], x["k8"], x["v8"], o, lse, scale, x["descale_q"],
+                                   x["descale_k"], x["descale_v"], args.causal)
+    elif args.profile == "decode_paged":
+        x = inputs.make_qkv(B, H, 1, N, d, 4242, with_do=False, device="cuda")
+        bs, nb = 256, N // 256
+        perm = torch.randperm(B * nb, generator=torch.Generator().manual_seed(7)).cuda()
+
+        def paged(t):
+            blocks = t.view(B, H, nb, bs, d).permute(0, 2, 3, 1, 4).reshape(B * nb, bs, H, d)
+            pool = torch.empty_like(blocks)
+            pool[perm] = blocks
+            return pool
+        kc, vc = paged(x["k"]), paged(x["v"])
+        table = perm.view(B, nb).to(torch.int32).contiguous()
+        seqlens = torch.full((B,), N, dtype=torch.int32, device="cuda")
+        o = torch.empty_like(x["q"])
+        lse = torch.empty((B, H, 1), dtype=torch.float32, device="cuda")
+        n_splits = max(1, N // 512)
+        ws = torch.empty(fa.fa_decode_workspace_size(B, H, N, d, n_splits), dtype=torch.uint8, device="cuda")
+        op = lambda: fa.fa_decode_paged(x["q"], kc, vc, o, lse, table, seqlens, N, scale, n_splits, ws)
+    elif args.profile == "decode":
         x = inputs.make_qkv(B, H, 1, N, d, 4242, with_do=False, device="cuda")
         o = torch.empty_like(x["q"])
         lse = torch.empty((B, H, 1), dtype=torch.float32, device="cuda")
@@ -657,7 +681,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
-    ap.add_argument("--profile", choices=("fwd", "bwd", "decode"), default=None,
+    ap.add_argument("--profile", choices=("fwd", "bwd", "decode", "fwd8", "decode_paged"), default=None,
                     help="run one op on a small case (for ncu) instead of the benchmark")
     ap.add_argument("--shape", default="2,32,4096,128", help="B,H,N,d for --profile")
     ap.add_argument("--causal", action="store_true", help="causal for --profile")
