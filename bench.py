@@ -412,7 +412,10 @@ def run_ours(args, rank, world, local_rank):
                           "ms": round(ms8, 4), "kernel_ms": round(k8, 4),
                           "frac_of_fp8_peak": round(fl / (k8 * 1e-3) / 1e12 / peak_f8, 4),
                           "fp8_peak": peak_f8,
-                          "peak_source": "2 x bf16_tflops (burst, measured): nominal fp8/bf16 ratio"}
+                          "peak_source": "2 x bf16_tflops (burst, measured): nominal fp8/bf16 ratio",
+                          "traffic": profiled_traffic("fwd_kernel<128, fp8>", source_digest(
+                              "exact_io_aware_08_gb300/csrc/fwd.cu", "exact_io_aware_08_gb300/csrc/sm103.cuh"))
+                          if not causal else None}
     del x8
 
     # ---- e2e through the public API with pinned host buffers (restore the headline inputs)
@@ -561,6 +564,8 @@ def run_ours(args, rank, world, local_rank):
         "gbps": round(whole_job_rate(bytes_dec, world, dp_ms * 1e-3) / 1e9, 1),
         "ms": round(dp_ms, 4), "frac_of_hbm": round(gbs_p / peak_hbm, 4),
         "kernels": "decode_split_kernel<128, paged> + decode_merge_kernel<128> (one call)",
+        "traffic": profiled_traffic("decode_split_kernel<128, paged>", source_digest(
+            "exact_io_aware_08_gb300/csrc/decode.cu", "exact_io_aware_08_gb300/csrc/sm103.cuh")),
     }
     clocks = sampler.stop()
     del qd, kc, vc
