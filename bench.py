@@ -12,6 +12,8 @@ Also measured in the same run and reported in the same JSON line:
   breakdown.decode         split-KV decode (B=64, H=32, N_kv=32768, d=128, 64 splits), GB/s
   breakdown.decode_paged   the same decode over a paged cache (256-key blocks, shuffled), GB/s
   breakdown.fwd_fp8*       forward from e4m3 Q, K, V (per-tensor scales), same shapes
+  breakdown.gpt2m_*        a GPT-2-medium attention layer, 8x16x1024x64 causal, fwd and fwd+bwd
+  breakdown.long_*         1x16x16384x128 causal with outlier keys, fwd and fwd+bwd
   breakdown.window         forward and forward+backward under a 4096-key causal sliding window
                            on 1x16x16384x128
   roofline                 the dominant kernel of the step (backward main kernel), timed alone
@@ -360,6 +362,52 @@ def run_ours(args, rank, world, local_rank):
                                    "ms": round(c_ms, 4)}
     breakdown["fwd_causal"] = {"tflops": round(whole_job_rate(fl_fc, world, cf_ms * 1e-3) / 1e12, 1),
                                "ms": round(cf_ms, 4)}
+
+    # ---- the other two training-direction workloads: a GPT-2-medium layer (8x16x1024x64,
+    # causal) and the long causal sequence with outlier keys (1x16x16384x128)
+    l2_flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for wx in (inputs.GPT2M, inputs.LONG):
+        xx = {k_: v_.to(dev) for k_, v_ in inputs.make_workload(wx).items()}
+        ox, lx = torch.empty_like(xx["q"]), torch.empty(xx["q"].shape[:3], dtype=torch.float32, device=dev)
+        gx = [torch.empty_like(xx["q"]) for _ in range(3)]
+        wsx = torch.empty(fa.fa_bwd_workspace_size(wx.B, wx.H, wx.N_q, wx.N_kv, wx.d), dtype=torch.uint8,
+                          device=dev)
+        flx_f = W.fwd_flops(wx.B, wx.H, wx.N_q, wx.N_kv, wx.d, wx.causal)
+        flx_b = W.bwd_flops(wx.B, wx.H, wx.N_q, wx.N_kv, wx.d, wx.causal)
+
+        small = wx is inputs.GPT2M       # its inputs fit in L2: flush before every timed call
+
+        def fx(pe, wx=wx, xx=xx, ox=ox, lx=lx, small=small):
+            if small:
+                l2_flush.zero_()
+            if pe is not None:
+                pe[0].record(stream)
+            fa.fa_fwd(xx["q"], xx["k"], xx["v"], ox, lx, wx.scale, wx.causal)
+            if pe is not None:
+                pe[1].record(stream)
+
+        def fbx(pe, wx=wx, xx=xx, ox=ox, lx=lx, gx=gx, wsx=wsx, small=small):
+            if small:
+                l2_flush.zero_()
+            if pe is not None:
+                pe[0].record(stream)
+            fa.fa_fwd(xx["q"], xx["k"], xx["v"], ox, lx, wx.scale, wx.causal)
+            fa.fa_bwd(xx["q"], xx["k"], xx["v"], ox, lx, xx["do"], gx[0], gx[1], gx[2], wsx, wx.scale,
+                      wx.causal)
+            if pe is not None:
+                pe[1].record(stream)
+        _, tf = timed(fx, K, inner=True)
+        _, tfb = timed(fbx, K, inner=True)
+        mf, mfb = reduce_max(statistics.mean(tf)), reduce_max(statistics.mean(tfb))
+        breakdown[wx.name] = {
+            "fwd_tflops": round(whole_job_rate(flx_f, world, mf * 1e-3) / 1e12, 1), "fwd_ms": round(mf, 4),
+            "fwd_bwd_tflops": round(whole_job_rate(flx_f + flx_b, world, mfb * 1e-3) / 1e12, 1),
+            "fwd_bwd_ms": round(mfb, 4),
+            "l2": "256 MB buffer written before every timed call (inputs fit in L2); per-call events"
+                  if small else "inputs exceed the 129 MB L2; per-call events",
+        }
+        del xx, ox, lx, gx, wsx
+    del l2_flush
 
     # ---- sliding window on the long sequence: 1x16x16384x128, each query sees its last 4096 keys
     wl_ = inputs.LONG
