@@ -24,6 +24,11 @@
 // O_0, O_1 (d each).  An S_t product is issued after the PV_t product that reads P_t from the
 // same columns; tcgen05.mma operations of one thread execute in issue order.
 //
+// Variants (template flags): VL -- packed variable-length batches (one work item per sequence,
+// head and 256-row block); F8 -- e4m3 Q, K, V (tcgen05.mma kind::f8f6f4, K = 32 per
+// instruction, P stored as e4m3 four per TMEM column over the first 32 columns of S_t); WIN --
+// a sliding window (each query tile streams only the key tiles its rows can see).
+//
 // Rescaling.  The online-softmax theorem holds for ANY reference value that l and o~ share:
 // o~/l is unchanged when both are measured against a stale maximum.  So a row moves its
 // reference m to the new running max only when the max grew by more than 2^8 (exp2 units);
@@ -51,7 +56,6 @@ struct FwdCfg {
   static constexpr int KS_S = D * EB / 32;            // 32-byte k-steps of S = Q K^T
   static constexpr int KS_PV = BN * EB / 32;          // 32-byte k-steps of O += P V
   static constexpr int PV_B_STEP = (32 / EB) * 128;   // V bytes per PV k-step (32/EB key rows)
-  static constexpr int P_COLS = BN * EB / 4;          // TMEM columns P occupies over S
   static constexpr int OFF_Q = 0;                     // Q_0, Q_1 (bf16: later O staging)
   static constexpr int OFF_K = 2 * TILE;
   static constexpr int OFF_V = OFF_K + NS * TILE;

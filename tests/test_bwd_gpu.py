@@ -120,3 +120,28 @@ def test_bwd_dk_dv_deterministic():
     a = run_fwd_bwd(x, True, 0.1)
     b = run_fwd_bwd(x, True, 0.1)
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+
+
+def test_long_workload_needs_no_n_by_n_buffer():
+    """1 x 16 x 16384 x 128 causal, forward + backward through the C ABI: the caller's buffers
+    (inputs, outputs, the O(N d) workspace) are all the memory the path touches -- far below one
+    N x N score matrix per head -- and the calls allocate nothing on the device."""
+    require_gpu()
+    w = inputs.LONG
+    x = {k: v.cuda() for k, v in inputs.make_workload(w).items()}
+    o = torch.empty_like(x["q"])
+    lse = torch.empty(x["q"].shape[:3], dtype=torch.float32, device="cuda")
+    grads = [torch.empty_like(x["q"]) for _ in range(3)]
+    ws = torch.empty(fa.fa_bwd_workspace_size(w.B, w.H, w.N_q, w.N_kv, w.d), dtype=torch.uint8,
+                     device="cuda")
+    caller_bytes = sum(t.numel() * t.element_size() for t in [*x.values(), o, lse, *grads, ws])
+    n_by_n_bf16 = w.B * w.H * w.N_q * w.N_kv * 2
+    assert caller_bytes < n_by_n_bf16 / 8
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    fa.fa_fwd(x["q"], x["k"], x["v"], o, lse, w.scale, True)
+    fa.fa_bwd(x["q"], x["k"], x["v"], o, lse, x["do"], *grads, ws, w.scale, True)
+    fa.fa_sync_status()
+    free_after = torch.cuda.mem_get_info()[0]
+    assert free_before - free_after < (64 << 20), (free_before, free_after)
+    assert all(torch.isfinite(t.float()).all() for t in (o, *grads))
