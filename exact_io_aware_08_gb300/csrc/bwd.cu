@@ -67,7 +67,7 @@ struct BwdCfg {
   static constexpr uint32_t T_S = 2 * D;
   static constexpr uint32_t T_DP = 2 * D + BM;
   static constexpr uint32_t T_DQ = 2 * D + 2 * BM;  // two dQ tile buffers of 64 columns
-  static constexpr int THREADS = 448;
+  static constexpr int THREADS = 480;             // + warp 14, the MMA thread's helper
   static constexpr int DS_THREADS = 256;          // two dS warpgroups
   static constexpr int HALF = BM / 2;             // query columns per dS warpgroup
   static_assert(T_DQ + 128 <= TMEM_COLS, "TMEM budget");
@@ -174,8 +174,9 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       mbar_init(&stage_empty[s], 1);
     }
     mbar_init(st_full, 1);
-    mbar_init(p_ready, C::DS_THREADS);
-    mbar_init(ds_ready, C::DS_THREADS);
+    // the dS threads + the helper warp's lane 0 (which folds in the other conditions)
+    mbar_init(p_ready, C::DS_THREADS + 1);
+    mbar_init(ds_ready, C::DS_THREADS + 1);
     mbar_init(pds_free, 1);
     for (int b2 = 0; b2 < 2; ++b2) {
       mbar_init(&dq_full[b2], 1);
@@ -289,12 +290,8 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
         for (int ks = 0; ks < C::BM / 16; ++ks)       // dV += P^T dO
           umma_ts(tbase + C::T_DV, tbase + C::T_S + ks * 8 + ((16 * ks) / C::HALF) * (C::HALF / 2),
                   desc_advance(do_mn, ks * 2048), id_acc, (i > 0 || ks > 0) ? 1u : 0u);
-        if (i + 1 < n) {
-          if (!(ok = mbar_wait(&stage_full[(i + 1) % C::NST], ((i + 1) / C::NST) & 1, abort_flag, 214)))
-            break;
-          tc_fence_after();
-          issue_s_dp(i + 1);
-        }
+        // stage i+1 is loaded: p_ready(i) includes the helper's check of it
+        if (i + 1 < n) issue_s_dp(i + 1);
         if (!(ok = mbar_wait(ds_ready, i & 1, abort_flag, 218))) break;
         tc_fence_after();
 #pragma unroll
@@ -303,11 +300,8 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
           umma_ss(tbase + C::T_DK, desc_advance(dDS, a_off), desc_advance(q_mn, ks * 2048), id_acc,
                   (i > 0 || ks > 0) ? 1u : 0u);
         }
-        const int qb = i & 1;                    // dQ TMEM buffer of this step
-        if (i >= 2) {
-          if (!(ok = mbar_wait(&dq_free[qb], ((i >> 1) - 1) & 1, abort_flag, 216))) break;
-          tc_fence_after();
-        }
+        // dQ TMEM buffer of this step, drained: ds_ready(i) includes the helper's check of it
+        const int qb = i & 1;
 #pragma unroll
         for (int ks = 0; ks < C::BN / 16; ++ks) {
           // d = 128: dQ^T = K^T dS^T (A = K as MN-major, B = dS^T as MN-major)
@@ -468,6 +462,27 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       }
       bulk_commit_group();
       bulk_wait_group_read0();
+    }
+  } else if (warp == 14) {
+    // ------------------------------------------------------------------ helper
+    // Each wait of the MMA thread costs the tensor core a bubble (even a completed mbarrier wait
+    // keeps the issuing thread ~150 cycles, and the queue ahead of it is short).  The MMA
+    // thread therefore waits only on p_ready and ds_ready; this thread folds the other
+    // conditions into them: stage i+1 loaded (needed by S/dP_{i+1}, issued after dV_i) and the
+    // dQ TMEM buffer of step i drained (needed by dQ_i).  It arrives on phase i of each barrier
+    // only after phase i-1 has completed, so its arrival cannot count for an earlier phase.
+    if (lane == 0) {
+      bool ok = true;
+      for (int i = 0; ok && i < n; ++i) {
+        if (i + 1 < n &&
+            !(ok = mbar_wait(&stage_full[(i + 1) % C::NST], ((i + 1) / C::NST) & 1, abort_flag, 240)))
+          break;
+        if (i > 0 && !(ok = mbar_wait(p_ready, (i - 1) & 1, abort_flag, 241))) break;
+        mbar_arrive(p_ready);
+        if (i >= 2 && !(ok = mbar_wait(&dq_free[i & 1], ((i >> 1) - 1) & 1, abort_flag, 242))) break;
+        if (i > 0 && !(ok = mbar_wait(ds_ready, (i - 1) & 1, abort_flag, 243))) break;
+        mbar_arrive(ds_ready);
+      }
     }
   } else {
     // ------------------------------------------------------------------ dQ warpgroup
