@@ -14,7 +14,10 @@
 //                 O_t += P_t V_j           A = P_t from TMEM, B = V_j from shared memory
 //               in the order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so the tensor core works
 //               on one tile while the other tile's softmax runs.
-//   warps 2-3   idle (they complete warpgroup 0, which gives up registers with setmaxnreg).
+//   warp 2      helper: folds "V_j loaded" and "K_{j+1} loaded" into the P hand-off (p_full), so
+//               the MMA thread waits once per tile and key tile (each wait of the issuing thread
+//               costs the tensor core a bubble).  Warp 3 is idle (warpgroup 0 gives up registers
+//               with setmaxnreg).
 //   warps 4-7   softmax of tile 0, warps 8-11 softmax of tile 1: thread = query row.  A thread
 //               loads its S row from TMEM, updates (m, l) in the log2 domain (scale * log2 e
 //               folded into one FMA), writes P as bf16 back over its S row in TMEM (P never
@@ -189,7 +192,7 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&s_full[t], 1);
-      mbar_init(&p_full[t], 128);
+      mbar_init(&p_full[t], 129);         // the tile's 128 softmax threads + the helper
       mbar_init(&o_done[t], 1);
     }
     *abort_flag = 0;
@@ -287,8 +290,7 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       // stream position j; tile t is on its i-th key tile, i = j - off[t]
       for (int j = 0; ok && j < n_max; ++j) {
         const int s = j % C::NS;
-        if (!(ok = mbar_wait(&v_full[s], (j / C::NS) & 1, abort_flag, 113))) break;
-        bool k_ready = false;
+        // V_j and K_{j+1} are loaded: the helper checked them before its p_full arrival
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           const int i = WIN ? j - off[t] : j;       // without a window both tiles start at 0
@@ -298,19 +300,36 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
             issue_pv(t, j, i == 0);
             if (i + 1 == n_t[t]) umma_commit(&o_done[t]);
           }
-          if ((!WIN || i + 1 >= 0) && i + 1 < n_t[t]) {
-            if (!k_ready) {
-              if (!(ok = mbar_wait(&k_full[(j + 1) % C::NS], ((j + 1) / C::NS) & 1, abort_flag, 114)))
-                break;
-              tc_fence_after();
-              k_ready = true;
-            }
-            issue_s(t, j + 1);
-          }
+          if ((!WIN || i + 1 >= 0) && i + 1 < n_t[t]) issue_s(t, j + 1);
         }
         if (!ok) break;
         umma_commit(&v_empty[s]);
         if (j + 1 < n_max) umma_commit(&k_empty[(j + 1) % C::NS]);
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------------ helper
+    if (lane == 0 && n_max > 0) {
+      bool ok = true;
+      for (int j = 0; ok && j < n_max; ++j) {
+        if (!(ok = mbar_wait(&v_full[j % C::NS], (j / C::NS) & 1, abort_flag, 130))) break;
+        bool k_next = false;                         // does some tile need S(j+1)?
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int i = WIN ? j - off[t] : j;
+          k_next |= (!WIN || i + 1 >= 0) && i + 1 < n_t[t];
+        }
+        if (k_next && !(ok = mbar_wait(&k_full[(j + 1) % C::NS], ((j + 1) / C::NS) & 1, abort_flag, 131)))
+          break;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int i = WIN ? j - off[t] : j;
+          if ((!WIN || i >= 0) && i < n_t[t]) {
+            // arrive on phase i only once phase i-1 is complete
+            if (i > 0 && !(ok = mbar_wait(&p_full[t], (i - 1) & 1, abort_flag, 132 + t))) break;
+            mbar_arrive(&p_full[t]);
+          }
+        }
       }
     }
   }
