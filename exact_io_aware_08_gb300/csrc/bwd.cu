@@ -47,18 +47,21 @@ struct BwdCfg {
   static constexpr int Q_CHUNK = BM * 128;          // [BM rows x 64 cols] swizzled
   static constexpr int DS_TILE = BN * BM * 2;       // dS^T, [QCH][128][64]
   static constexpr int NST = 3;
-  static constexpr int STAGE = 2 * Q_TILE + 1024;   // Q, dO, then lse2[BM], delta[BM]
+  static constexpr int STAGE = 2 * Q_TILE;          // Q, dO (swizzled, 1 KB aligned)
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = KV_TILE;
   static constexpr int OFF_ST = 2 * KV_TILE;
   static constexpr int OFF_DS = OFF_ST + NST * STAGE;
   // d = 128: staging of one fp32 dQ tile [BM queries][d] for the TMA reduce-add into dQ_acc
   static constexpr int DQS_BYTES = (D == 128) ? BM * D * 4 : 0;
-  static constexpr int OFF_DQS = OFF_DS + DS_TILE;
-  static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
-  // kv_full, stage_full[NST], stage_empty[NST], st_full, p_ready, ds_ready, pds_free,
+  static constexpr int OFF_DQS = OFF_DS + 2 * DS_TILE;      // dS^T double-buffered
+  // per stage: -lse log2e [BM], -D [BM] (fp32), written by the producer warp
+  static constexpr int OFF_LSE = OFF_DQS + DQS_BYTES;
+  static constexpr int LSE_STAGE = 2 * BM * 4;
+  static constexpr int OFF_BAR = OFF_LSE + NST * LSE_STAGE;
+  // kv_full, stage_full[NST], stage_empty[NST], st_full, p_ready, ds_ready, pds_free[2],
   // dq_full[2], dq_free[2], mma_done, dqs_sync
-  static constexpr int NBAR = 1 + 2 * NST + 10;
+  static constexpr int NBAR = 1 + 2 * NST + 11;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -71,6 +74,7 @@ struct BwdCfg {
   static constexpr int DS_THREADS = 256;          // two dS warpgroups
   static constexpr int HALF = BM / 2;             // query columns per dS warpgroup
   static_assert(T_DQ + 128 <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget (227 KB per CTA)");
 };
 
 struct BwdParams {
@@ -117,8 +121,8 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
   uint64_t* st_full = stage_empty + C::NST;
   uint64_t* p_ready = st_full + 1;       // P^T of the step is in TMEM (dV may start)
   uint64_t* ds_ready = p_ready + 1;      // dS^T of the step is in shared memory (dK, dQ may start)
-  uint64_t* pds_free = ds_ready + 1;
-  uint64_t* dq_full = pds_free + 1;      // [2], one per dQ TMEM buffer
+  uint64_t* pds_free = ds_ready + 1;     // [2], one per dS^T buffer
+  uint64_t* dq_full = pds_free + 2;      // [2], one per dQ TMEM buffer
   uint64_t* dq_free = dq_full + 2;       // [2]
   uint64_t* mma_done = dq_free + 2;
   uint64_t* dqs_sync = mma_done + 1;     // the four dQ warps around the staging buffer
@@ -173,11 +177,14 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       mbar_init(&stage_full[s], 2);      // TMA bytes + the producer warp's lse/D writes
       mbar_init(&stage_empty[s], 1);
     }
-    mbar_init(st_full, 1);
+    // st_full: the MMA's commit + the helper, which folds in "stage i loaded" (lse, D) and
+    // "dS^T buffer i & 1 free" (dK, dQ of step i-2 done) so the dS warps wait once per step
+    mbar_init(st_full, 2);
     // the dS threads + the helper warp's lane 0 (which folds in the other conditions)
     mbar_init(p_ready, C::DS_THREADS + 1);
     mbar_init(ds_ready, C::DS_THREADS + 1);
-    mbar_init(pds_free, 1);
+    mbar_init(&pds_free[0], 1);
+    mbar_init(&pds_free[1], 1);
     for (int b2 = 0; b2 < 2; ++b2) {
       mbar_init(&dq_full[b2], 1);
       mbar_init(&dq_free[b2], 128);
@@ -224,7 +231,7 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
                         y2(q_beg, q0));
           }
         }
-        float* s_lse = reinterpret_cast<float*>(st + 2 * C::Q_TILE);
+        float* s_lse = reinterpret_cast<float*>(smem + C::OFF_LSE + s * C::LSE_STAGE);
         float* s_del = s_lse + C::BM;
         for (int e = lane; e < C::BM; e += 32) {
           const int q = q0 + e;
@@ -297,7 +304,7 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
 #pragma unroll
         for (int ks = 0; ks < C::BM / 16; ++ks) {     // dK += dS^T Q
           const uint32_t a_off = (ks >> 2) * C::KV_CHUNK + (ks & 3) * 32;
-          umma_ss(tbase + C::T_DK, desc_advance(dDS, a_off), desc_advance(q_mn, ks * 2048), id_acc,
+          umma_ss(tbase + C::T_DK, desc_advance(dDS, (i & 1) * C::DS_TILE + a_off), desc_advance(q_mn, ks * 2048), id_acc,
                   (i > 0 || ks > 0) ? 1u : 0u);
         }
         // dQ TMEM buffer of this step, drained: ds_ready(i) includes the helper's check of it
@@ -307,12 +314,12 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
           // d = 128: dQ^T = K^T dS^T (A = K as MN-major, B = dS^T as MN-major)
           // d = 64:  dQ   = dS K     (A = dS^T as MN-major, B = K as MN-major)
           const uint64_t kd = desc_advance(dK_mn, ks * 2048);
-          const uint64_t dd = desc_advance(dDS_mn, ks * 2048);
+          const uint64_t dd = desc_advance(dDS_mn, (i & 1) * C::DS_TILE + ks * 2048);
           if constexpr (D == 128) umma_ss(tbase + C::T_DQ + qb * 64, kd, dd, id_dq, ks > 0);
           else umma_ss(tbase + C::T_DQ + qb * 64, dd, kd, id_dq, ks > 0);
         }
         umma_commit(&dq_full[qb]);
-        umma_commit(pds_free);
+        umma_commit(&pds_free[i & 1]);
         umma_commit(&stage_empty[s]);
       }
       umma_commit(mma_done);
@@ -331,11 +338,11 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
     bool ok = true;
     for (int i = 0; i < n; ++i) {
       const int q0 = (i_start + i) * C::BM;
+      // st_full(i): S/dP_i are done, stage i (lse, D) is loaded and dS^T buffer i & 1 is free
+      // (the last two folded in by the helper)
       if (!(ok = mbar_wait_warp(st_full, i & 1, abort_flag, 221))) break;
-      // lse/D of this stage were written by the producer warp: acquire them directly
-      if (!(ok = mbar_wait_warp(&stage_full[i % C::NST], (i / C::NST) & 1, abort_flag, 224))) break;
       tc_fence_after();
-      const float* s_nlse = reinterpret_cast<const float*>(stage_ptr(i % C::NST) + 2 * C::Q_TILE);
+      const float* s_nlse = reinterpret_cast<const float*>(smem + C::OFF_LSE + (i % C::NST) * C::LSE_STAGE);
       const float* s_nd = s_nlse + C::BM;
       // a (key tile, query tile) pair that some pair of rows sees only in part
       const bool diag = WIN ? ((q0 < k0 + C::BN - 1 - wr) || (q0 + C::BM - 1 > k0 + wl))
@@ -398,12 +405,12 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
                                 fadd2(make_float2(dpf[e], dpf[e + 1]), make_float2(ndf[e], ndf[e + 1])));
         pk_ds[e / 2] = pack_bf16x2(ds.x, ds.y);
       }
-      if (i > 0 && !(ok = mbar_wait_warp(pds_free, (i - 1) & 1, abort_flag, 222))) break;
+      uint8_t* sDSi = sDS + (i & 1) * C::DS_TILE;
 #pragma unroll
       for (int u = 0; u < C::HALF / 8; ++u) {
         const int c8 = cb / 8 + u;                   // 16-byte unit along the query axis
         const uint32_t off = (c8 >> 3) * C::KV_CHUNK + sw128_offset(r, (c8 & 7) * 8);
-        *reinterpret_cast<uint4*>(sDS + off) =
+        *reinterpret_cast<uint4*>(sDSi + off) =
             make_uint4(pk_ds[4 * u], pk_ds[4 * u + 1], pk_ds[4 * u + 2], pk_ds[4 * u + 3]);
       }
       fence_proxy_async_smem();
@@ -474,6 +481,11 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
     if (lane == 0) {
       bool ok = true;
       for (int i = 0; ok && i < n; ++i) {
+        // st_full phase i: stage i loaded, dS^T buffer i & 1 free (dK, dQ of step i-2 done)
+        if (!(ok = mbar_wait(&stage_full[i % C::NST], (i / C::NST) & 1, abort_flag, 244))) break;
+        if (i >= 2 && !(ok = mbar_wait(&pds_free[i & 1], ((i >> 1) - 1) & 1, abort_flag, 245))) break;
+        if (i > 0 && !(ok = mbar_wait(st_full, (i - 1) & 1, abort_flag, 246))) break;
+        mbar_arrive(st_full);
         if (i + 1 < n &&
             !(ok = mbar_wait(&stage_full[(i + 1) % C::NST], ((i + 1) / C::NST) & 1, abort_flag, 240)))
           break;
