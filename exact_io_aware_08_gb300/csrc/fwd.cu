@@ -83,6 +83,14 @@ struct FwdCfg {
   // range (e4m3 is normal down to 2^-6).
   static constexpr float RESCALE_THRESHOLD = F8 ? 4.f : 8.f;
   static constexpr float P_BIAS = F8 ? 4.f : 0.f;
+  // fp8: the P hand-off of tile t is named barrier BAR_P + t (one generation per P V product:
+  // the tile's 128 softmax threads arrive, the MMA and helper warps sync).  An mbarrier wait
+  // costs the issuing thread ~150 cycles even when the phase is complete, which at the fp8
+  // tile rate leaves the tensor core idle; the hardware barrier does not.  (Measured: fp8
+  // 0.59 -> 0.56 ms; the bf16 forward was slower with it, so it keeps the mbarrier.)
+  static constexpr bool NAMED_P = F8;
+  static constexpr uint32_t BAR_P = 3;
+  static constexpr uint32_t BAR_P_THREADS = 128 + 32 + 32;
 };
 
 struct FwdParams {
@@ -242,6 +250,104 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
         }
       }
     }
+  } else if (C::NAMED_P && warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer (fp8)
+    // The whole warp walks the loop (it takes part in the named-barrier hand-offs); lane 0
+    // issues.  After a failed wait the warp keeps joining every hand-off, issuing nothing.
+    if (n_max > 0) {
+      const bool leader = lane == 0;
+      // Q, K both K-major; P from TMEM, V MN-major
+      const uint32_t idesc_s = F8 ? idesc_e4m3_f32(128, 128, 0, 0) : idesc_bf16_f32(128, 128, 0, 0);
+      const uint32_t idesc_o = F8 ? idesc_e4m3_f32(128, D, 0, 1) : idesc_bf16_f32(128, D, 0, 1);
+      // Descriptors are built once; each k-step adds a compile-time offset (desc_advance).
+      const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 0, 1024);
+      const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 0, 1024);
+      const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), C::CHUNK, 1024);
+      auto issue_s = [&](int t, int j) {                        // S_t = Q_t K_j^T
+        const uint64_t a = desc_advance(dq0, t * C::TILE);
+        const uint64_t b = desc_advance(dk0, (j % C::NS) * C::TILE);
+        const uint32_t d_tmem = tbase + C::T_S + t * 128;
+#pragma unroll
+        for (int ks = 0; ks < C::KS_S; ++ks) {
+          const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
+          if constexpr (F8)
+            umma_ss_f8(d_tmem, desc_advance(a, off), desc_advance(b, off), idesc_s, ks > 0);
+          else
+            umma_ss(d_tmem, desc_advance(a, off), desc_advance(b, off), idesc_s, ks > 0);
+        }
+        umma_commit(&s_full[t]);
+      };
+      auto issue_pv = [&](int t, int j, bool first) {           // O_t += P_t V_j
+        const uint64_t b = desc_advance(dv0, (j % C::NS) * C::TILE);
+        const uint32_t d_tmem = tbase + C::T_O + t * D;
+        const uint32_t a_tmem = tbase + C::T_S + t * 128;
+#pragma unroll
+        for (int ks = 0; ks < C::KS_PV; ++ks) {
+          if constexpr (F8)
+            umma_ts_f8(d_tmem, a_tmem + ks * 8, desc_advance(b, ks * C::PV_B_STEP), idesc_o,
+                       (!first || ks > 0) ? 1u : 0u);
+          else
+            umma_ts(d_tmem, a_tmem + ks * 8, desc_advance(b, ks * C::PV_B_STEP), idesc_o,
+                    (!first || ks > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait_warp(q_full, 0, abort_flag, 111) && mbar_wait_warp(&k_full[0], 0, abort_flag, 112);
+      if (ok && leader) {
+        tc_fence_after();
+        if (n_t[0] > 0) issue_s(0, 0);
+        if (n_t[1] > 0 && (!WIN || off[1] == 0)) issue_s(1, 0);
+        umma_commit(&k_empty[0]);
+      }
+      // stream position j; tile t is on its i-th key tile, i = j - off[t]
+      for (int j = 0; j < n_max; ++j) {
+        const int s = j % C::NS;
+        // V_j and K_{j+1} are loaded: the helper checked them before joining the hand-off
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int i = WIN ? j - off[t] : j;       // without a window both tiles start at 0
+          if ((!WIN || i >= 0) && i < n_t[t]) {
+            __syncwarp();
+            named_bar_sync(C::BAR_P + t, C::BAR_P_THREADS);
+            if (ok && leader) {
+              tc_fence_after();
+              issue_pv(t, j, i == 0);
+              if (i + 1 == n_t[t]) umma_commit(&o_done[t]);
+            }
+          }
+          if (ok && leader && (!WIN || i + 1 >= 0) && i + 1 < n_t[t]) issue_s(t, j + 1);
+        }
+        if (ok && leader) {
+          umma_commit(&v_empty[s]);
+          if (j + 1 < n_max) umma_commit(&k_empty[(j + 1) % C::NS]);
+        }
+      }
+    }
+  } else if (C::NAMED_P && warp == 2) {
+    // ------------------------------------------------------------------ helper (fp8)
+    // Joins each P hand-off once V_j (and K_{j+1}, if an S(j+1) follows) is loaded, so the MMA
+    // warp's single wait per hand-off also covers the loads.  The whole warp takes part; after
+    // a failed wait it keeps joining every remaining hand-off.
+    if (n_max > 0) {
+      bool ok = true;
+      for (int j = 0; j < n_max; ++j) {
+        bool k_next = false;                         // does some tile need S(j+1)?
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int i = WIN ? j - off[t] : j;
+          k_next |= (!WIN || i + 1 >= 0) && i + 1 < n_t[t];
+        }
+        if (ok) ok = mbar_wait_warp(&v_full[j % C::NS], (j / C::NS) & 1, abort_flag, 130);
+        if (ok && k_next) ok = mbar_wait_warp(&k_full[(j + 1) % C::NS], ((j + 1) / C::NS) & 1, abort_flag, 131);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int i = WIN ? j - off[t] : j;
+          if ((!WIN || i >= 0) && i < n_t[t]) {
+            __syncwarp();
+            named_bar_sync(C::BAR_P + t, C::BAR_P_THREADS);
+          }
+        }
+      }
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0 && n_max > 0) {
@@ -355,6 +461,7 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
     float l = 0.f;                            // sum of 2^{(s - m) c2} over keys seen (fp32)
     float lb = 0.f;                           // the same sum over the bf16-rounded weights
     bool ok = true;
+    int handed = 0;                           // fp8: P hand-offs joined so far
 
     for (int j = 0; j < n; ++j) {
       if (!(ok = mbar_wait_warp(&s_full[t], j & 1, abort_flag, 121))) break;
@@ -470,7 +577,21 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       lb += rb01.x + rb01.y;
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[t]);
+      if constexpr (C::NAMED_P) {
+        __syncwarp();
+        named_bar_arrive(C::BAR_P + t, C::BAR_P_THREADS);
+        ++handed;
+      } else {
+        mbar_arrive(&p_full[t]);
+      }
+    }
+    // fp8, after an abort: keep joining the remaining hand-offs (blocking, so these arrivals
+    // cannot run ahead of a generation the MMA and helper warps have not completed)
+    if constexpr (C::NAMED_P) {
+      for (; handed < n; ++handed) {
+        __syncwarp();
+        named_bar_sync(C::BAR_P + t, C::BAR_P_THREADS);
+      }
     }
 
     // ------------------------------------------------------------------ epilogue

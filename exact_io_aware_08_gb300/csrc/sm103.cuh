@@ -47,6 +47,15 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
 }
 
+// Named-barrier hand-off (the hardware barrier unit, no shared-memory traffic: a waiting
+// issuing thread does not fall behind the tensor core the way an mbarrier wait does).  Both
+// are .aligned: the whole warp executes them together (callers __syncwarp() first).  A named
+// barrier cannot time out, so every participant must take part in every generation; the
+// kernels that use them keep participating (without work) after an abort.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.arrive %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ uint32_t elect_one_sync() {
   uint32_t pred = 0;
   asm volatile(
