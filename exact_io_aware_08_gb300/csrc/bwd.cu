@@ -10,7 +10,7 @@
 // TMEM, written once), query tiles stream, and dQ is accumulated across key tiles in fp32.
 //
 //   F2  bwd_pre:   D = rowsum(dO o O) in fp32; zero the fp32 dQ accumulator.
-//   F3  bwd_main:  one CTA per (128-key tile, head); 448 threads:
+//   F3  bwd_main:  one CTA per (128-key tile, head); 480 threads:
 //         warp 0     TMA producer: K_j, V_j once; Q_i, dO_i (+ lse_i, D_i) per query tile
 //                    through a 3-deep ring.
 //         warp 1     TMEM owner and MMA issuer: S^T = K Q^T, dP^T = V dO^T (keys on TMEM
@@ -21,8 +21,12 @@
 //                    P^T (bf16) goes back into TMEM over the S^T columns just read; dS^T
 //                    (bf16) goes to shared memory, where the dK and dQ products read it.
 //                    Epilogue: one group writes dV, the other dK (times scale), via TMA.
-//         warps 10-13 drain the dQ tile from TMEM into the fp32 accumulator with vector
-//                    reductions (red.global.add), overlapping the next tile's MMAs.
+//         warps 10-13 drain the dQ tile from TMEM into the fp32 accumulator, overlapping the
+//                    next tile's MMAs: d = 128 through a row-major fp32 box in shared memory
+//                    and one TMA reduce-add per step, d = 64 with vector reductions
+//                    (red.global.add).
+//         warp 14    helper: folds the waits that do not depend on the dS math (stage loaded,
+//                    dS^T and dQ buffers free) into the hand-offs the MMA thread waits on.
 //       TMEM (512 columns): dV, dK (d each), S^T, dP^T (BM each), two dQ tiles (64 each), so
 //       the dQ drain of step i overlaps the dQ product of step i+1.
 //       d = 128 uses 64-query steps and forms dQ^T = K^T dS^T (d on TMEM lanes);
@@ -361,15 +365,16 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
         uint32_t rs[32], rd[32];
         tmem_ld32(tbase + t_lane + C::T_S + cb + c * 32, rs);
         tmem_ld32(tbase + t_lane + C::T_DP + cb + c * 32, rd);
-        // per-column -lse (log2 units) and -D: the same for every thread (broadcast reads)
+        // per-column -lse (log2 units) and -D, the same for every thread: lane l reads column
+        // l once and shuffles pass the values round (a uniform-address shared load costs a
+        // shared-memory wavefront per 4 bytes delivered)
         float nl[32];
+        const float lane_nl = s_nlse[cb + c * 32 + lane];
+        const float lane_nd = s_nd[cb + c * 32 + lane];
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 a = *reinterpret_cast<const float4*>(s_nlse + cb + c * 32 + e);
-          const float4 b4 = *reinterpret_cast<const float4*>(s_nd + cb + c * 32 + e);
-          nl[e] = a.x; nl[e + 1] = a.y; nl[e + 2] = a.z; nl[e + 3] = a.w;
-          ndf[c * 32 + e] = b4.x; ndf[c * 32 + e + 1] = b4.y;
-          ndf[c * 32 + e + 2] = b4.z; ndf[c * 32 + e + 3] = b4.w;
+        for (int e = 0; e < 32; ++e) {
+          nl[e] = __shfl_sync(0xffffffffu, lane_nl, e);
+          ndf[c * 32 + e] = __shfl_sync(0xffffffffu, lane_nd, e);
         }
         tmem_wait_ld();
         uint32_t pk_p[16];
