@@ -63,9 +63,9 @@ struct BwdCfg {
   static constexpr int OFF_LSE = OFF_DQS + DQS_BYTES;
   static constexpr int LSE_STAGE = 2 * BM * 4;
   static constexpr int OFF_BAR = OFF_LSE + NST * LSE_STAGE;
-  // kv_full, stage_full[NST], stage_empty[NST], st_full, p_ready, ds_ready, pds_free[2],
-  // dq_full[2], dq_free[2], mma_done, dqs_sync
-  static constexpr int NBAR = 1 + 2 * NST + 11;
+  // kv_full, stage_full[NST], stage_empty[NST], st_full, dp_full, p_ready, ds_ready,
+  // pds_free[2], dq_full[2], dq_free[2], mma_done, dqs_sync
+  static constexpr int NBAR = 1 + 2 * NST + 12;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
@@ -123,7 +123,8 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
   uint64_t* stage_full = bars + 1;
   uint64_t* stage_empty = stage_full + C::NST;
   uint64_t* st_full = stage_empty + C::NST;
-  uint64_t* p_ready = st_full + 1;       // P^T of the step is in TMEM (dV may start)
+  uint64_t* dp_full = st_full + 1;       // dP^T of the step is in TMEM (committed after S^T)
+  uint64_t* p_ready = dp_full + 1;       // P^T of the step is in TMEM (dV may start)
   uint64_t* ds_ready = p_ready + 1;      // dS^T of the step is in shared memory (dK, dQ may start)
   uint64_t* pds_free = ds_ready + 1;     // [2], one per dS^T buffer
   uint64_t* dq_full = pds_free + 2;      // [2], one per dQ TMEM buffer
@@ -184,6 +185,7 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
     // st_full: the MMA's commit + the helper, which folds in "stage i loaded" (lse, D) and
     // "dS^T buffer i & 1 free" (dK, dQ of step i-2 done) so the dS warps wait once per step
     mbar_init(st_full, 2);
+    mbar_init(dp_full, 1);
     // the dS threads + the helper warp's lane 0 (which folds in the other conditions)
     mbar_init(p_ready, C::DS_THREADS + 1);
     mbar_init(ds_ready, C::DS_THREADS + 1);
@@ -271,14 +273,21 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
         const uint32_t st = (i % C::NST) * C::STAGE;
         const uint64_t q_k = desc_advance(dST_k, st);
         const uint64_t do_k = desc_advance(dST_k, st + C::Q_TILE);
+        // S^T first and committed on its own, so the dS warps exponentiate while dP^T runs
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t kv_off = (ks >> 2) * C::KV_CHUNK + (ks & 3) * 32;
           const uint32_t q_off = (ks >> 2) * C::Q_CHUNK + (ks & 3) * 32;
           umma_ss(tbase + C::T_S, desc_advance(dK_k, kv_off), desc_advance(q_k, q_off), id_s, ks > 0);
-          umma_ss(tbase + C::T_DP, desc_advance(dV_k, kv_off), desc_advance(do_k, q_off), id_s, ks > 0);
         }
         umma_commit(st_full);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t kv_off = (ks >> 2) * C::KV_CHUNK + (ks & 3) * 32;
+          const uint32_t q_off = (ks >> 2) * C::Q_CHUNK + (ks & 3) * 32;
+          umma_ss(tbase + C::T_DP, desc_advance(dV_k, kv_off), desc_advance(do_k, q_off), id_s, ks > 0);
+        }
+        umma_commit(dp_full);
       };
       bool ok = mbar_wait(kv_full, 0, abort_flag, 211) &&
                 mbar_wait(&stage_full[0], 0, abort_flag, 212);
@@ -342,8 +351,8 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
     bool ok = true;
     for (int i = 0; i < n; ++i) {
       const int q0 = (i_start + i) * C::BM;
-      // st_full(i): S/dP_i are done, stage i (lse, D) is loaded and dS^T buffer i & 1 is free
-      // (the last two folded in by the helper)
+      // st_full(i): S_i is done, stage i (lse, D) is loaded and dS^T buffer i & 1 is free
+      // (the last two folded in by the helper); dp_full(i), waited for below: dP_i is done
       if (!(ok = mbar_wait_warp(st_full, i & 1, abort_flag, 221))) break;
       tc_fence_after();
       const float* s_nlse = reinterpret_cast<const float*>(smem + C::OFF_LSE + (i % C::NST) * C::LSE_STAGE);
@@ -359,23 +368,20 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       // dV product reads it.  p_ready is signalled as soon as every thread has stored its P^T
       // and read its dP^T, so dV and the next S/dP products (which overwrite S^T and dP^T)
       // overlap the dS math below.
-      float pf[C::HALF], dpf[C::HALF], ndf[C::HALF];
+      float pf[C::HALF], lane_nd[C::HALF / 32];
+      uint32_t dpu[C::HALF / 32][32];
 #pragma unroll
       for (int c = 0; c < C::HALF / 32; ++c) {
-        uint32_t rs[32], rd[32];
+        uint32_t rs[32];
         tmem_ld32(tbase + t_lane + C::T_S + cb + c * 32, rs);
-        tmem_ld32(tbase + t_lane + C::T_DP + cb + c * 32, rd);
         // per-column -lse (log2 units) and -D, the same for every thread: lane l reads column
         // l once and shuffles pass the values round (a uniform-address shared load costs a
         // shared-memory wavefront per 4 bytes delivered)
         float nl[32];
         const float lane_nl = s_nlse[cb + c * 32 + lane];
-        const float lane_nd = s_nd[cb + c * 32 + lane];
+        lane_nd[c] = s_nd[cb + c * 32 + lane];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          nl[e] = __shfl_sync(0xffffffffu, lane_nl, e);
-          ndf[c * 32 + e] = __shfl_sync(0xffffffffu, lane_nd, e);
-        }
+        for (int e = 0; e < 32; ++e) nl[e] = __shfl_sync(0xffffffffu, lane_nl, e);
         tmem_wait_ld();
         uint32_t pk_p[16];
 #pragma unroll
@@ -394,20 +400,25 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
           }
           pf[c * 32 + e] = p0;
           pf[c * 32 + e + 1] = p1;
-          dpf[c * 32 + e] = __uint_as_float(rd[e]);
-          dpf[c * 32 + e + 1] = __uint_as_float(rd[e + 1]);
           pk_p[e / 2] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tbase + t_lane + C::T_S + cb + c * 16, pk_p);
       }
+      if (!(ok = mbar_wait_warp(dp_full, i & 1, abort_flag, 224))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < C::HALF / 32; ++c) tmem_ld32(tbase + t_lane + C::T_DP + cb + c * 32, dpu[c]);
+      tmem_wait_ld();
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_ready);
       // dS^T = P^T o (dP^T - D)
 #pragma unroll
       for (int e = 0; e < C::HALF; e += 2) {
-        const float2 ds = fmul2(make_float2(pf[e], pf[e + 1]),
-                                fadd2(make_float2(dpf[e], dpf[e + 1]), make_float2(ndf[e], ndf[e + 1])));
+        const float2 dp = make_float2(__uint_as_float(dpu[e / 32][e % 32]), __uint_as_float(dpu[e / 32][e % 32 + 1]));
+        const float2 nd = make_float2(__shfl_sync(0xffffffffu, lane_nd[e / 32], e % 32),
+                                      __shfl_sync(0xffffffffu, lane_nd[e / 32], e % 32 + 1));
+        const float2 ds = fmul2(make_float2(pf[e], pf[e + 1]), fadd2(dp, nd));
         pk_ds[e / 2] = pack_bf16x2(ds.x, ds.y);
       }
       uint8_t* sDSi = sDS + (i & 1) * C::DS_TILE;
