@@ -137,9 +137,11 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work item: key tile kt of head bh; causal key tiles with more query tiles run first.
-  const int bh = blockIdx.x / p.n_kvtiles;           // fixed length: (b, h) plane
-  const int kt = blockIdx.x % p.n_kvtiles;
+  // Work item: key tile kt of head bh; causal key tiles with more query tiles run first,
+  // across groups of kCausalGroup heads.
+  int bh = blockIdx.x / p.n_kvtiles;                 // fixed length: (b, h) plane
+  int kt = blockIdx.x % p.n_kvtiles;
+  if (!VL && !WIN && p.causal) causal_item(blockIdx.x, gridDim.x / p.n_kvtiles, p.n_kvtiles, &bh, &kt);
   const int k0 = kt * C::BN;
   int n_q = p.n_q, n_kv = p.n_kv, q_beg = 0, k_beg = 0, head = 0;
   if (VL) {

@@ -20,6 +20,23 @@ enum DevError : unsigned int {
 // i - win_left <= j <= i + win_right.
 constexpr int kWinUnbounded = 1 << 30;
 
+// Causal work items differ in length (a query pair or key tile near the start of a head has
+// the most partners).  The kernels map blockIdx so that items run longest-first across groups
+// of this many heads: the CTAs that start last are short ones, while the heads in flight
+// (about one group and a half) keep their K/V or Q/dO in L2.
+constexpr int kCausalGroup = 8;
+
+// (head, rank) of CTA ``block`` in a grid of n_bh heads x per_head items: rank 0 first across
+// the heads of a group, then rank 1, ...  A bijection onto [0, n_bh) x [0, per_head).
+__device__ __forceinline__ void causal_item(int block, int n_bh, int per_head, int* bh, int* rank) {
+  const int per_group = kCausalGroup * per_head;
+  const int g0 = (block / per_group) * kCausalGroup;
+  const int g = min(kCausalGroup, n_bh - g0);          // heads in this (possibly last) group
+  const int w = block - (g0 / kCausalGroup) * per_group;
+  *rank = w / g;
+  *bh = g0 + w % g;
+}
+
 // Window of a call: an explicit window (win_left / win_right >= 0 or kWinUnbounded) when
 // ``windowed``, else causal = (unbounded, 0) or no mask = (unbounded, unbounded).
 inline void attention_window(int causal, bool windowed, int left, int right, int* wl, int* wr) {

@@ -137,11 +137,13 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
   const int lane = threadIdx.x & 31;
 
   // Work item: query rows [256 c, 256 c + 256) of head bh.  Items of one head are adjacent so
-  // the CTAs that run together share K/V in L2; causal runs each head's longer items first.
+  // the CTAs that run together share K/V in L2; causal items run longest-first across groups
+  // of kCausalGroup heads.
   // Variable-length: item = (sequence, head, 256-row block), sized by the longest sequence;
   // blocks past a sequence's end exit at once.  Rows are then local to the sequence.
-  const int bh = blockIdx.x / p.n_qpairs;             // fixed length: (b, h) plane
-  const int r = blockIdx.x % p.n_qpairs;
+  int bh = blockIdx.x / p.n_qpairs;                   // fixed length: (b, h) plane
+  int r = blockIdx.x % p.n_qpairs;
+  if (!VL && !WIN && p.causal) causal_item(blockIdx.x, gridDim.x / p.n_qpairs, p.n_qpairs, &bh, &r);
   int n_q = p.n_q, n_kv = p.n_kv, q_beg = 0, k_beg = 0, head = 0;
   if (VL) {
     const int seq = bh / p.heads;

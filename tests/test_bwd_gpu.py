@@ -40,6 +40,8 @@ SHAPES = [
     (1, 2, 1000, 1000, 128, True),
     (1, 1, 1, 130, 128, False),
     (1, 1, 640, 640, 64, True),
+    (3, 4, 700, 700, 128, True),     # 12 heads: causal items ordered across a full and a partial group
+    (3, 3, 300, 300, 64, True),      # 9 heads, d = 64
 ]
 
 

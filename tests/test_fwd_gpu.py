@@ -34,6 +34,8 @@ SHAPES = [
     (1, 1, 129, 129, 128, True),
     (2, 2, 384, 384, 64, False),
     (1, 1, 640, 640, 128, False),
+    (3, 4, 700, 700, 128, True),     # 12 heads: causal items ordered across a full and a partial group
+    (3, 3, 300, 300, 64, True),      # 9 heads, d = 64
 ]
 
 
