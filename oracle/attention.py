@@ -34,7 +34,9 @@ Readings where the pages leave a step open:
   * tau is the caller's ``scale`` (one page prints QK^T/d, having lost the square root);
   * causal means query i sees keys j <= i, with N_q == N_kv (Lesson4 "Causal masks");
   * a row that sees no key has lse = -inf and O = 0, never NaN (Lesson4 §3 "Compute it stably");
-  * lse is the natural logarithm.
+  * lse is the natural logarithm;
+  * block-sparse attention (Scratch "Results" names it, with no pattern) is the plain definition
+    under a 0/1 mask over (query block, key block) pairs, ANDed with the causal mask if asked.
 """
 from __future__ import annotations
 
@@ -436,5 +438,86 @@ def forward_window_rows(q_rows, row_index, k, v, scale: float, left: int, right:
         vis &= j >= i - left
     if right >= 0:
         vis &= j <= i + right
+    p, m, l = three_pass_softmax(np.where(vis, s, NEG_INF))
+    return p @ v, lse_from(m, l)
+
+
+# --------------------------------------------------------------------------------------------
+# Block-sparse attention
+# --------------------------------------------------------------------------------------------
+# [Scratch] "Results" names a block-sparse variant of the method (the same IO-aware tiling
+# applied to a sparse pattern) without fixing a pattern.  Reading taken: a 0/1 mask over
+# (query block, key block) pairs of a fixed block size; attention is the plain definition over
+# the keys of the set blocks, and with ``causal`` also only j <= i ([Lesson4] "Causal masks");
+# a row that sees no key gets O = 0 and lse = -inf, as for an empty key set.  The mask is either
+# one [n_qblocks, n_kblocks] array for every head or one per head, [B, H, n_qblocks, n_kblocks].
+
+def block_visible(block_mask, n_q: int, n_kv: int, block: int, causal: bool) -> np.ndarray:
+    """Boolean [n_q, n_kv]: True where mask[i // block, j // block] is set (and j <= i if causal)."""
+    bm = np.asarray(block_mask).astype(bool)
+    i = np.arange(n_q)[:, None]
+    j = np.arange(n_kv)[None, :]
+    vis = bm[i // block, j // block]
+    if causal:
+        vis = vis & (j <= i)
+    return vis
+
+
+def _mask_of_head(block_mask, b: int, h: int):
+    m = np.asarray(block_mask)
+    return m if m.ndim == 2 else m[b, h]
+
+
+def forward_block_sparse_head(q, k, v, scale: float, block_mask, block: int, causal: bool):
+    """One head under a block mask: returns (O, lse, P)."""
+    s = scale * (q @ k.T)
+    s = np.where(block_visible(block_mask, q.shape[0], k.shape[0], block, causal), s, NEG_INF)
+    p, m, l = three_pass_softmax(s)
+    return p @ v, lse_from(m, l), p
+
+
+def forward_block_sparse(q, k, v, scale: float, block_mask, causal: bool = False, block: int = 128):
+    """Block-sparse forward over [B, H, N, d]; fp64 (O, lse)."""
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    B, H, n_q, _ = q.shape
+    o = np.zeros((B, H, n_q, v.shape[-1]))
+    lse = np.full((B, H, n_q), NEG_INF)
+    for b in range(B):
+        for h in range(H):
+            o[b, h], lse[b, h], _ = forward_block_sparse_head(
+                q[b, h], k[b, h], v[b, h], scale, _mask_of_head(block_mask, b, h), block, causal)
+    return o, lse
+
+
+def backward_block_sparse(q, k, v, do, scale: float, block_mask, causal: bool = False,
+                          block: int = 128):
+    """Block-sparse gradients: the backward formulas of ``backward_head`` with the masked P
+    (scores outside the set blocks have P = 0 and contribute nothing)."""
+    q, k, v, do = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(do)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    for b in range(q.shape[0]):
+        for h in range(q.shape[1]):
+            _, _, p = forward_block_sparse_head(q[b, h], k[b, h], v[b, h], scale,
+                                                _mask_of_head(block_mask, b, h), block, causal)
+            dv[b, h] = p.T @ do[b, h]
+            dp = do[b, h] @ v[b, h].T
+            D = (p * dp).sum(axis=-1)
+            ds = p * (dp - D[:, None])
+            dq[b, h] = scale * (ds @ k[b, h])
+            dk[b, h] = scale * (ds.T @ q[b, h])
+    return dq, dk, dv
+
+
+def forward_block_sparse_rows(q_rows, row_index, k, v, scale: float, block_mask, causal: bool,
+                              block: int = 128):
+    """Block-sparse forward for selected query rows of one head (full-size sampling): the same
+    definition as ``forward_block_sparse_head`` evaluated for a subset of independent rows."""
+    q_rows, k, v = _as_f64(q_rows), _as_f64(k), _as_f64(v)
+    s = scale * (q_rows @ k.T)
+    i = np.asarray(row_index)[:, None]
+    j = np.arange(k.shape[0])[None, :]
+    vis = np.asarray(block_mask).astype(bool)[i // block, j // block]
+    if causal:
+        vis = vis & (j <= i)
     p, m, l = three_pass_softmax(np.where(vis, s, NEG_INF))
     return p @ v, lse_from(m, l)

@@ -500,3 +500,111 @@ def test_window_rows_match_full_head():
         o_r, lse_r = A.forward_window_rows(q[0, 1, rows], rows, k[0, 1], v[0, 1], 0.3, left, right)
         np.testing.assert_allclose(o_r, o[rows], atol=1e-14)
         np.testing.assert_allclose(lse_r, lse[rows], atol=1e-14)
+
+
+# ---------------------------------------------------------------------------- block-sparse
+def _elem_mask_torch(bm, n, block, causal):
+    """Element mask built independently of the oracle: repeat each block entry block x block."""
+    import torch
+    m = torch.from_numpy(np.asarray(bm).astype(bool))
+    m = m.repeat_interleave(block, 0).repeat_interleave(block, 1)[:n, :n]
+    if causal:
+        m = m & torch.ones(n, n, dtype=torch.bool).tril()
+    return m
+
+
+BS_MASK = np.array([[1, 0, 0, 1, 0, 1, 0, 1, 1, 0],
+                    [1, 1, 0, 0, 0, 0, 1, 0, 0, 1],
+                    [0, 1, 1, 0, 1, 0, 0, 0, 1, 0],
+                    [1, 0, 0, 1, 0, 0, 0, 1, 0, 0],
+                    [0, 0, 1, 0, 1, 1, 0, 0, 0, 1],
+                    [1, 0, 0, 0, 0, 1, 1, 0, 1, 0],
+                    [0, 1, 0, 1, 0, 0, 1, 0, 0, 0],
+                    [0, 0, 0, 0, 1, 0, 1, 1, 0, 1],
+                    [1, 0, 1, 0, 0, 0, 0, 0, 1, 0],
+                    [0, 1, 0, 0, 1, 0, 0, 1, 0, 1]], dtype=np.uint8)   # not symmetric, full diagonal
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_sparse_vs_torch_sdpa_boolean_mask(causal):
+    import torch
+    q, k, v, _ = _qkv(6, N=37)                       # block 4: ten blocks, the last one ragged
+    o, lse = A.forward_block_sparse(q, k, v, 0.3, BS_MASK, causal, block=4)
+    mask = _elem_mask_torch(BS_MASK, 37, 4, causal)
+    qt, kt, vt = (torch.from_numpy(t) for t in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=0.3)
+    np.testing.assert_allclose(o, ref.numpy(), atol=1e-13)
+    s = (0.3 * qt @ kt.transpose(-1, -2)).masked_fill(~mask, float("-inf"))
+    np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).numpy(), atol=1e-13)
+
+
+def test_block_sparse_all_ones_reduces_to_plain_attention():
+    q, k, v, _ = _qkv(7, N=37)
+    ones = np.ones((10, 10), dtype=np.uint8)
+    for causal in (False, True):
+        o, lse = A.forward_block_sparse(q, k, v, 0.3, ones, causal, block=4)
+        o_ref, lse_ref = A.forward(q, k, v, 0.3, causal)
+        np.testing.assert_allclose(o, o_ref, atol=1e-14)
+        np.testing.assert_allclose(lse, lse_ref, atol=1e-13)
+
+
+def test_block_diagonal_mask_is_attention_within_each_segment():
+    q, k, v, _ = _qkv(8, N=37)
+    eye = np.eye(10, dtype=np.uint8)
+    o, lse = A.forward_block_sparse(q, k, v, 0.3, eye, False, block=4)
+    for a in range(0, 37, 4):
+        b = min(a + 4, 37)
+        o_ref, lse_ref = A.forward(q[:, :, a:b], k[:, :, a:b], v[:, :, a:b], 0.3, False)
+        np.testing.assert_allclose(o[:, :, a:b], o_ref, atol=1e-14)
+        np.testing.assert_allclose(lse[:, :, a:b], lse_ref, atol=1e-13)
+
+
+def test_block_sparse_empty_block_row_gives_zero_and_neg_inf():
+    q, k, v, do = _qkv(9, N=20)
+    bm = np.ones((5, 5), dtype=np.uint8)
+    bm[2] = 0                                          # queries 8..11 see nothing
+    o, lse = A.forward_block_sparse(q, k, v, 0.3, bm, False, block=4)
+    assert (o[:, :, 8:12] == 0).all() and np.isneginf(lse[:, :, 8:12]).all()
+    assert np.isfinite(lse[:, :, :8]).all() and np.isfinite(lse[:, :, 12:]).all()
+    dq, dk, dv = A.backward_block_sparse(q, k, v, do, 0.3, bm, False, block=4)
+    assert (dq[:, :, 8:12] == 0).all()
+    assert np.isfinite(dq).all() and np.isfinite(dk).all() and np.isfinite(dv).all()
+
+
+def test_block_sparse_per_head_masks():
+    q, k, v, _ = _qkv(10, B=2, H=2, N=37)
+    g = np.random.default_rng(3)
+    per = (g.random((2, 2, 10, 10)) < 0.5).astype(np.uint8)
+    per[..., np.arange(10), np.arange(10)] = 1
+    o, lse = A.forward_block_sparse(q, k, v, 0.3, per, True, block=4)
+    for b in range(2):
+        for h in range(2):
+            o1, lse1 = A.forward_block_sparse(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1],
+                                              0.3, per[b, h], True, block=4)
+            np.testing.assert_array_equal(o[b, h], o1[0, 0])
+            np.testing.assert_array_equal(lse[b, h], lse1[0, 0])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_sparse_backward_vs_torch_autograd(causal):
+    import torch
+    q, k, v, do = _qkv(11, N=29)                     # every row sees its own diagonal block
+    dq, dk, dv = A.backward_block_sparse(q, k, v, do, 0.3, BS_MASK[:8, :8], causal, block=4)
+    mask = _elem_mask_torch(BS_MASK[:8, :8], 29, 4, causal)
+    qt, kt, vt = (torch.from_numpy(t).requires_grad_() for t in (q, k, v))
+    out = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=0.3)
+    out.backward(torch.from_numpy(do))
+    np.testing.assert_allclose(dq, qt.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dk, kt.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dv, vt.grad.numpy(), atol=1e-12)
+
+
+def test_block_sparse_rows_match_full_head():
+    q, k, v, _ = _qkv(12, N=37)
+    rows = np.array([0, 5, 17, 36])
+    for causal in (False, True):
+        o, lse, _ = A.forward_block_sparse_head(q[0, 1], k[0, 1], v[0, 1], 0.3, BS_MASK, 4, causal)
+        o_r, lse_r = A.forward_block_sparse_rows(q[0, 1, rows], rows, k[0, 1], v[0, 1], 0.3, BS_MASK,
+                                                 causal, block=4)
+        np.testing.assert_allclose(o_r, o[rows], atol=1e-14)
+        np.testing.assert_allclose(lse_r, lse[rows], atol=1e-14)

@@ -144,6 +144,21 @@ def _window_sides_swapped(n_q, n_kv, left, right):
     return vis
 
 
+def _block_visible_transposed(block_mask, n_q, n_kv, block, causal):
+    bm = np.asarray(block_mask).astype(bool)
+    i = np.arange(n_q)[:, None]
+    j = np.arange(n_kv)[None, :]
+    vis = bm[j // block, i // block]                             # mask indexed (key, query)
+    return vis & (j <= i) if causal else vis
+
+
+def _block_visible_no_causal(block_mask, n_q, n_kv, block, causal):
+    bm = np.asarray(block_mask).astype(bool)
+    i = np.arange(n_q)[:, None]
+    j = np.arange(n_kv)[None, :]
+    return bm[i // block, j // block]                            # drops the causal part
+
+
 # the pins each mutation is run against (any failing one is a catch)
 FWD_PINS = [
     lambda: P.test_forward_vs_torch_sdpa_fp64((2, 3, 37, 37, 16), False),
@@ -183,6 +198,13 @@ WINDOW_PINS = [
     lambda: P.test_window_backward_vs_torch_autograd(2, 5),
 ]
 
+BLOCK_PINS = [
+    lambda: P.test_block_sparse_vs_torch_sdpa_boolean_mask(False),
+    lambda: P.test_block_sparse_vs_torch_sdpa_boolean_mask(True),
+    P.test_block_sparse_all_ones_reduces_to_plain_attention,
+    P.test_block_diagonal_mask_is_attention_within_each_segment,
+]
+
 MUTATIONS = [
     ("scores", _scores_no_scale, FWD_PINS),
     ("scores", _scores_mask(lambda i, j: j < i), FWD_PINS),
@@ -203,6 +225,8 @@ MUTATIONS = [
     ("forward_fp8", _fp8_swapped_scales, FP8_PINS),
     ("window_visible", _window_off_by_one, WINDOW_PINS),
     ("window_visible", _window_sides_swapped, WINDOW_PINS),
+    ("block_visible", _block_visible_transposed, BLOCK_PINS),
+    ("block_visible", _block_visible_no_causal, BLOCK_PINS),
 ]
 
 
