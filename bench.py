@@ -16,6 +16,8 @@ Also measured in the same run and reported in the same JSON line:
   breakdown.long_*         1x16x16384x128 causal with outlier keys, fwd and fwd+bwd
   breakdown.window         forward and forward+backward under a 4096-key causal sliding window
                            on 1x16x16384x128
+  breakdown.block_sparse   the same shape under a causal 128x128 block pattern (a band of one
+                           block, the first key block, 5% random blocks)
   roofline                 the dominant kernel of the step (backward main kernel), timed alone
   e2e                      the step through the public Python API with host (pinned) buffers,
                            host->device and device->host copies inside the timed region
@@ -437,7 +439,32 @@ def run_ours(args, rank, world, local_rank):
         "fwd_bwd_ms": round(ws_ms, 4),
         "flops": "4 d (fwd) and 10 d (bwd) per visible (query, key) pair",
     }
-    del xw, ow, lw, gw, wsw
+    # ---- block-sparse on the same long sequence: 128 x 128 blocks, a band of one block either
+    # side of the diagonal, the first key block and 5% random blocks, causal inside the blocks
+    bmask = inputs.make_block_mask(-(-wl_.N_q // fa.BLOCK_SIZE), -(-wl_.N_kv // fa.BLOCK_SIZE), 1005)
+    bpairs = W.block_sparse_pairs(bmask, wl_.N_q, wl_.N_kv, True) * wl_.B * wl_.H
+    bmask_d = bmask.to(dev)
+    fl_bf, fl_bb = 4 * wl_.d * bpairs, 10 * wl_.d * bpairs
+
+    def bs_fwd(pe):
+        fa.fa_fwd_block_sparse(xw["q"], xw["k"], xw["v"], ow, lw, wl_.scale, bmask_d, True)
+
+    def bs_step(pe):
+        bs_fwd(pe)
+        fa.fa_bwd_block_sparse(xw["q"], xw["k"], xw["v"], ow, lw, xw["do"], gw[0], gw[1], gw[2], wsw,
+                               wl_.scale, bmask_d, True)
+    bf_total, _ = timed(bs_fwd, K)
+    bb_total, _ = timed(bs_step, K)
+    bf_ms, bb_ms = reduce_max(bf_total / K), reduce_max(bb_total / K)
+    breakdown["block_sparse"] = {
+        "workload": f"{wl_.name} under a causal block-sparse pattern (128x128 blocks: band of 1, first "
+                    f"key block, 5% random; {float(bmask.float().mean()):.3f} of blocks set)",
+        "fwd_tflops": round(whole_job_rate(fl_bf, world, bf_ms * 1e-3) / 1e12, 1), "fwd_ms": round(bf_ms, 4),
+        "fwd_bwd_tflops": round(whole_job_rate(fl_bf + fl_bb, world, bb_ms * 1e-3) / 1e12, 1),
+        "fwd_bwd_ms": round(bb_ms, 4),
+        "flops": "4 d (fwd) and 10 d (bwd) per visible (query, key) pair",
+    }
+    del xw, ow, lw, gw, wsw, bmask_d
 
     # ---- FP8 forward (e4m3 Q, K, V with per-tensor scales) on the same shapes
     x8 = inputs.make_qkv_fp8(w.B, w.H, w.N_q, w.N_kv, w.d, w.seed + 7919 * rank, device=str(dev))

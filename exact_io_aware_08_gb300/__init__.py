@@ -21,7 +21,11 @@ __all__ = [
     "forward", "backward", "decode", "fa_fwd_varlen", "forward_varlen",
     "fa_bwd_varlen", "backward_varlen", "fa_decode_paged", "decode_paged", "fa_fwd_fp8", "forward_fp8",
     "fa_fwd_window", "fa_bwd_window", "forward_window", "backward_window",
+    "fa_fwd_block_sparse", "fa_bwd_block_sparse", "forward_block_sparse", "backward_block_sparse",
+    "BLOCK_SIZE",
 ]
+
+BLOCK_SIZE = 128   # block-sparse attention: blocks of 128 queries x 128 keys
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libfa.so")
@@ -63,6 +67,9 @@ _SIGNATURES = {
     "fa_decode_splitkv_noalloc": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _P]),
     "fa_fwd_window": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P]),
     "fa_bwd_window": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _F, _I, _I, _P]),
+    "fa_fwd_block_sparse": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _I, _P]),
+    "fa_bwd_block_sparse": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _S, _I, _I, _I, _I, _I, _F,
+                                 _I, _P, _I, _P]),
     "fa_fwd_fp8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _F, _F, _I, _P]),
     "fa_decode_paged": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _S,
                              _P]),
@@ -249,6 +256,38 @@ def fa_bwd_window(q, k, v, o, lse, do, dq, dk, dv, ws, scale: float, window_left
                                         _stream(stream)))
 
 
+def _mask_args(block_mask, B, H):
+    """(pointer, per_head) of a uint8 device block mask: [nqb, nkb] shared or [B, H, nqb, nkb]."""
+    per_head = 1 if block_mask.dim() == 4 else 0
+    if per_head and tuple(block_mask.shape[:2]) != (B, H):
+        raise FaError(1, f"per-head block mask must be [B, H, nqb, nkb], got {tuple(block_mask.shape)}")
+    if not block_mask.is_contiguous():
+        raise FaError(1, "block mask must be contiguous")
+    return _ptr(block_mask), per_head
+
+
+def fa_fwd_block_sparse(q, k, v, o, lse, scale: float, block_mask, causal: bool = False, stream=None):
+    """block_mask: uint8 on the device, [ceil(N_q/128), ceil(N_kv/128)] or per head
+    [B, H, ceil(N_q/128), ceil(N_kv/128)]; nonzero = block computed."""
+    B, H, n_q, d = q.shape
+    n_kv = k.shape[2]
+    mp, per_head = _mask_args(block_mask, B, H)
+    _check(load_library().fa_fwd_block_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H,
+                                              n_q, n_kv, d, float(scale), int(bool(causal)), mp,
+                                              per_head, _stream(stream)))
+
+
+def fa_bwd_block_sparse(q, k, v, o, lse, do, dq, dk, dv, ws, scale: float, block_mask,
+                        causal: bool = False, stream=None):
+    B, H, n_q, d = q.shape
+    n_kv = k.shape[2]
+    mp, per_head = _mask_args(block_mask, B, H)
+    _check(load_library().fa_bwd_block_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do),
+                                              _ptr(dq), _ptr(dk), _ptr(dv), _ptr(ws), _nbytes(ws), B,
+                                              H, n_q, n_kv, d, float(scale), int(bool(causal)), mp,
+                                              per_head, _stream(stream)))
+
+
 def fa_fwd_fp8(q8, k8, v8, o, lse, scale: float, descale_q: float, descale_k: float,
                descale_v: float, causal: bool = False, stream=None):
     """q8, k8, v8: e4m3 codes (uint8 or float8_e4m3fn tensors) [B,H,N,d]; o bf16, lse fp32."""
@@ -386,4 +425,30 @@ def backward_window(q, k, v, o, lse, do, window_left: int, window_right: int,
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     fa_bwd_window(q, k, v, o, lse, do, dq, dk, dv, workspace, scale, window_left, window_right, stream)
+    return dq, dk, dv
+
+
+def forward_block_sparse(q, k, v, block_mask, causal: bool = False, scale: float | None = None,
+                         stream=None):
+    """Block-sparse forward (blocks of 128 x 128; see fa_fwd_block_sparse) -> (O, lse)."""
+    import torch
+    d = q.shape[-1]
+    scale = d ** -0.5 if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=q.device)
+    fa_fwd_block_sparse(q, k, v, o, lse, scale, block_mask, causal, stream)
+    return o, lse
+
+
+def backward_block_sparse(q, k, v, o, lse, do, block_mask, causal: bool = False,
+                          scale: float | None = None, stream=None, workspace=None):
+    """Block-sparse backward -> (dQ, dK, dV) in bf16."""
+    import torch
+    B, H, n_q, d = q.shape
+    scale = d ** -0.5 if scale is None else scale
+    need = fa_bwd_workspace_size(B, H, n_q, k.shape[2], d)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fa_bwd_block_sparse(q, k, v, o, lse, do, dq, dk, dv, workspace, scale, block_mask, causal, stream)
     return dq, dk, dv

@@ -78,3 +78,27 @@ def window_fwd_flops(B: int, H: int, n: int, d: int, left: int, right: int) -> i
 
 def window_bwd_flops(B: int, H: int, n: int, d: int, left: int, right: int) -> int:
     return 10 * d * window_pairs(n, left, right) * B * H
+
+
+def block_sparse_pairs(block_mask, n_q: int, n_kv: int, causal: bool, block: int = 128) -> int:
+    """Visible (query, key) pairs under a 0/1 block mask ([n_qblocks, n_kblocks] for one head,
+    or [..., n_qblocks, n_kblocks] summed over the leading axes), with causal (n_q == n_kv) also
+    j <= i: per set block its clipped rows x columns, a diagonal block only its lower triangle."""
+    import numpy as np
+    m = np.asarray(block_mask).astype(bool)
+    m = m.reshape(-1, m.shape[-2], m.shape[-1]).sum(axis=0)   # set count per block over heads
+    total = 0
+    for qb in range(m.shape[0]):
+        rows = min(block, n_q - qb * block)
+        for kb in range(m.shape[1]):
+            if not m[qb, kb]:
+                continue
+            cols = min(block, n_kv - kb * block)
+            if causal and kb > qb:
+                continue
+            if causal and kb == qb:
+                per = sum(min(i + 1, cols) for i in range(rows))
+            else:
+                per = rows * cols
+            total += int(m[qb, kb]) * per
+    return total

@@ -251,6 +251,70 @@ fa_status_t fa_bwd_window(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_
   return FA_OK;
 }
 
+// Block-sparse calls: the mask must exist (unless a side is empty) and cover at most
+// kBlockSparseMaxTiles key blocks.
+static fa_status_t check_block_mask(const unsigned char* block_mask, int mask_per_head, int N_q,
+                                    int N_kv) {
+  if (mask_per_head != 0 && mask_per_head != 1)
+    return fail(FA_ERR_INVALID_ARG, "mask_per_head must be 0 or 1 (got %d)", mask_per_head);
+  if (N_q > 0 && N_kv > 0 && !block_mask) return fail(FA_ERR_INVALID_ARG, "null block_mask");
+  const int kb = (N_kv + fa::kBlockSize - 1) / fa::kBlockSize;
+  if (kb > fa::kBlockSparseMaxTiles)
+    return fail(FA_ERR_UNSUPPORTED, "block-sparse attention covers at most %d key blocks (N_kv <= %d; got %d)",
+                fa::kBlockSparseMaxTiles, fa::kBlockSparseMaxTiles * fa::kBlockSize, N_kv);
+  return FA_OK;
+}
+
+fa_status_t fa_fwd_block_sparse(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
+                                fa_bf16_t* o, float* lse, int B, int H, int N_q, int N_kv, int d,
+                                float scale, int causal, const unsigned char* block_mask,
+                                int mask_per_head, void* stream) {
+  fa_status_t st = check_shape(B, H, N_q, N_kv, d, scale);
+  if (st != FA_OK) return st;
+  if (causal && N_q != N_kv)
+    return fail(FA_ERR_UNSUPPORTED, "causal requires N_q == N_kv (got %d, %d)", N_q, N_kv);
+  st = check_block_mask(block_mask, mask_per_head, N_q, N_kv);
+  if (st != FA_OK) return st;
+  if (N_q == 0) return FA_OK;
+  if (!q || !o || !lse || (N_kv > 0 && (!k || !v)))
+    return fail(FA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return fail(FA_ERR_INVALID_ARG, "arrays must be 16-byte aligned");
+  fa::FwdArgs a{q, k ? k : q, v ? v : q, o, lse, B, H, N_q, N_kv, d, scale, causal ? 1 : 0};
+  if (N_kv == 0) {
+    a.k = q;                             // no key at all: the plain kernel writes O = 0, lse = -inf
+    a.v = q;
+  } else {
+    a.block_mask = reinterpret_cast<const uint8_t*>(block_mask);
+    a.bm_per_head = mask_per_head;
+  }
+  cudaError_t e = fa::launch_fwd(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_block_sparse launch");
+  return FA_OK;
+}
+
+fa_status_t fa_bwd_block_sparse(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
+                                const fa_bf16_t* o, const float* lse, const fa_bf16_t* dO,
+                                fa_bf16_t* dq, fa_bf16_t* dk, fa_bf16_t* dv, void* ws,
+                                size_t ws_bytes, int B, int H, int N_q, int N_kv, int d,
+                                float scale, int causal, const unsigned char* block_mask,
+                                int mask_per_head, void* stream) {
+  fa::BwdArgs a;
+  const void* const ptrs[9] = {q, k, v, o, lse, dO, dq, dk, dv};
+  fa_status_t st = check_bwd(ptrs, kNeedAll, ws, ws_bytes, B, H, N_q, N_kv, d, scale, causal, &a);
+  if (st != FA_OK) return st;
+  st = check_block_mask(block_mask, mask_per_head, N_q, N_kv);
+  if (st != FA_OK) return st;
+  a.block_mask = reinterpret_cast<const uint8_t*>(block_mask);
+  a.bm_per_head = mask_per_head;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = fa::launch_bwd_prep(a, s);
+  if (e == cudaSuccess) e = fa::launch_bwd_main(a, s);
+  if (e == cudaSuccess) e = fa::launch_bwd_finish(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_bwd_block_sparse launch");
+  return FA_OK;
+}
+
 fa_status_t fa_bwd_prep(const fa_bf16_t* o, const fa_bf16_t* dO, void* ws, size_t ws_bytes,
                         int B, int H, int N_q, int N_kv, int d, void* stream) {
   fa::BwdArgs a;

@@ -98,6 +98,10 @@ struct BwdParams {
   uint16_t* dv;
   // Visible keys of query i: i - win_left <= j <= i + win_right (kWinUnbounded: no bound).
   int win_left, win_right;
+  // Block-sparse: 0/1 per (128-query block, 128-key block) pair, [n_qblocks][n_kvtiles] for
+  // every head (bm_per_head = 0) or one such array per (b, h) plane.
+  const uint8_t* block_mask;
+  int bm_per_head, n_qblocks;
 };
 
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
@@ -109,7 +113,7 @@ __device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float
                :: "l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
 }
 
-template <int D, bool VL, bool WIN = false>
+template <int D, bool VL, bool WIN = false, bool BS = false>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
 bwd_main_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
@@ -167,7 +171,40 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
   const int wl = min(p.win_left, kWinUnbounded - C::BN);
   const int i_start = WIN ? max(0, k0 - wr) / C::BM : (p.causal ? (k0 / C::BM) : 0);
   const int i_end = WIN ? min(n_qtiles, (k0 + C::BN - 1 + wl) / C::BM + 1) : n_qtiles;
-  const int n = max(0, i_end - i_start);
+  int n = max(0, i_end - i_start);
+  // Block-sparse: the steps are those of the query blocks whose block with this key tile is set
+  // (with causal, on or below the diagonal), in order, 128 / BM steps each (fewer for a ragged
+  // last block).  Warp 14 counts them before the roles start; each role that needs a step's
+  // first query walks the mask column with its own cursor (step_q0, called once per step).
+  const uint8_t* bs_col = nullptr;
+  if constexpr (BS)
+    bs_col = p.block_mask + static_cast<size_t>(p.bm_per_head ? bh : 0) * p.n_qblocks * p.n_kvtiles + kt;
+  auto bs_set = [&](int qb) {
+    return bs_col[static_cast<size_t>(qb) * p.n_kvtiles] != 0 && (!p.causal || qb >= kt);
+  };
+  auto bs_steps = [&](int qb) { return min(kBlockSize / C::BM, (n_q - qb * kBlockSize + C::BM - 1) / C::BM); };
+  int bs_qb = -1, bs_sub = 0;
+  auto step_q0 = [&](int i) -> int {
+    if constexpr (BS) {
+      if (bs_qb < 0 || ++bs_sub >= bs_steps(bs_qb)) {
+        bs_sub = 0;
+        do { ++bs_qb; } while (bs_qb < p.n_qblocks && !bs_set(bs_qb));
+      }
+      return bs_qb * kBlockSize + bs_sub * C::BM;
+    } else {
+      return (i_start + i) * C::BM;
+    }
+  };
+  if constexpr (BS) {
+    if (warp == 14) {
+      int cnt = 0;
+      for (int base = 0; base < p.n_qblocks; base += 32) {
+        const int qb = base + lane;
+        cnt += __reduce_add_sync(0xffffffffu, (qb < p.n_qblocks && bs_set(qb)) ? bs_steps(qb) : 0);
+      }
+      if (lane == 0) *reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8) = cnt;
+    }
+  }
   // TMA coordinates of local row ``row``: fixed length {x, row, (b,h)}; packed {x, h, beg+row}
   auto y1 = [&](int row) { return VL ? head : row; };
   auto y2 = [&](int beg, int row) { return VL ? beg + row : bh; };
@@ -212,6 +249,7 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  if constexpr (BS) n = *reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
@@ -230,7 +268,7 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
         const uint32_t u = i / C::NST;
         if (u > 0 && !(ok = mbar_wait_warp(&stage_empty[s], (u - 1) & 1, abort_flag, 201))) break;
         uint8_t* st = stage_ptr(s);
-        const int q0 = (i_start + i) * C::BM;
+        const int q0 = step_q0(i);
         if (lane == 0) {
           mbar_arrive_expect_tx(&stage_full[s], 2 * C::Q_TILE);
           for (int c = 0; c < C::KCH; ++c) {
@@ -352,7 +390,7 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
     const float c2 = p.scale_log2;
     bool ok = true;
     for (int i = 0; i < n; ++i) {
-      const int q0 = (i_start + i) * C::BM;
+      const int q0 = step_q0(i);
       // st_full(i): S_i is done, stage i (lse, D) is loaded and dS^T buffer i & 1 is free
       // (the last two folded in by the helper); dp_full(i), waited for below: dP_i is done
       if (!(ok = mbar_wait_warp(st_full, i & 1, abort_flag, 221))) break;
@@ -527,7 +565,7 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       const bool leader = threadIdx.x == 320;
       uint32_t use = 0;                              // dqs_sync phases used so far
       for (int i = 0; i < n; ++i) {
-        const int q0 = (i_start + i) * C::BM;
+        const int q0 = step_q0(i);
         const int qb = i & 1;
         if (!mbar_wait_warp(&dq_full[qb], (i >> 1) & 1, abort_flag, 231)) break;
         tc_fence_after();
@@ -556,7 +594,7 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       if (leader) bulk_wait_group0();
     } else {
       for (int i = 0; i < n; ++i) {
-        const int q0 = (i_start + i) * C::BM;
+        const int q0 = step_q0(i);
         const int qb = i & 1;
         if (!mbar_wait_warp(&dq_full[qb], (i >> 1) & 1, abort_flag, 231)) break;
         tc_fence_after();
@@ -683,8 +721,18 @@ static cudaError_t launch_bwd_main_d(const BwdArgs& a, cudaStream_t stream) {
   p.dk = static_cast<uint16_t*>(a.dk);
   p.dv = static_cast<uint16_t*>(a.dv);
   attention_window(a.causal, a.windowed, a.win_left, a.win_right, &p.win_left, &p.win_right);
+  p.block_mask = a.block_mask;
+  p.bm_per_head = a.bm_per_head;
+  p.n_qblocks = (a.n_q + kBlockSize - 1) / kBlockSize;
   static int attr_done[64] = {0};   // one per instantiation of this launcher
   const uint64_t grid = static_cast<uint64_t>(p.n_kvtiles) * bh;
+  if (a.block_mask != nullptr) {
+    static int attr_bs[64] = {0};
+    cudaError_t e = ensure_smem_attr(bwd_main_kernel<D, false, false, true>, C::SMEM_BYTES, attr_bs);
+    if (e != cudaSuccess) return e;
+    bwd_main_kernel<D, false, false, true><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError();
+  }
   if (a.windowed) {
     static int attr_win[64] = {0};
     cudaError_t e = ensure_smem_attr(bwd_main_kernel<D, false, true>, C::SMEM_BYTES, attr_win);
@@ -735,6 +783,8 @@ static cudaError_t launch_bwd_main_varlen_d(const BwdArgs& a, cudaStream_t strea
   p.dk = static_cast<uint16_t*>(a.dk);
   p.dv = static_cast<uint16_t*>(a.dv);
   attention_window(a.causal, false, 0, 0, &p.win_left, &p.win_right);
+  p.block_mask = nullptr;
+  p.bm_per_head = p.n_qblocks = 0;
   static int attr_done[64] = {0};
   cudaError_t e = ensure_smem_attr(bwd_main_kernel<D, true>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;

@@ -20,6 +20,11 @@ enum DevError : unsigned int {
 // i - win_left <= j <= i + win_right.
 constexpr int kWinUnbounded = 1 << 30;
 
+// Block-sparse attention: blocks are 128 queries x 128 keys, and a call covers at most this
+// many key blocks (N_kv <= 131072), the length of the per-CTA stream list kept on chip.
+constexpr int kBlockSize = 128;
+constexpr int kBlockSparseMaxTiles = 1024;
+
 // Causal work items differ in length (a query pair or key tile near the start of a head has
 // the most partners).  The kernels map blockIdx so that items run longest-first across groups
 // of this many heads: the CTAs that start last are short ones, while the heads in flight
@@ -56,6 +61,8 @@ struct FwdArgs {
   float descale_q = 1.f, descale_k = 1.f, descale_v = 1.f;   // fp8 forward only
   bool windowed = false;                                     // sliding window (below)
   int win_left = kWinUnbounded, win_right = kWinUnbounded;
+  const uint8_t* block_mask = nullptr;                       // block-sparse (device, below)
+  int bm_per_head = 0;
 };
 
 struct FwdVarlenArgs {
@@ -93,6 +100,8 @@ struct BwdArgs {
   int n_seqs = 0, total_q = 0, total_k = 0, max_seqlen_q = 0, max_seqlen_k = 0;
   bool windowed = false;                                     // sliding window (as FwdArgs)
   int win_left = kWinUnbounded, win_right = kWinUnbounded;
+  const uint8_t* block_mask = nullptr;                       // block-sparse (as FwdArgs)
+  int bm_per_head = 0;
 };
 
 struct DecodeArgs {

@@ -67,8 +67,11 @@ struct FwdCfg {
   static constexpr int OFF_BAR = F8 ? OFF_OST + 2 * OTILE : OFF_V + NS * TILE;
   // q_full, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[2], p_full[2], o_done[2]
   static constexpr int NBAR = 1 + 4 * NS + 6;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;   // + slack for 1 KB alignment
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;      // TMEM slot, abort flag, list length
+  // block-sparse: the CTA's key-tile stream (int16 indices) and which query tile wants each
+  static constexpr int OFF_BSL = OFF_MISC + 16;
+  static constexpr int OFF_BSB = OFF_BSL + 2 * kBlockSparseMaxTiles;
+  static constexpr int SMEM_BYTES = OFF_BSB + kBlockSparseMaxTiles + 1024;   // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t T_S = 0;                  // S_t at columns [128 t, 128 t + 128)
   static constexpr uint32_t T_O = 256;                // O_t at columns [256 + d t, ...)
@@ -110,9 +113,13 @@ struct FwdParams {
   // Visible keys of query i: i - win_left <= j <= i + win_right (kWinUnbounded = no bound on
   // that side).  Causal is (kWinUnbounded, 0), no mask (kWinUnbounded, kWinUnbounded).
   int win_left, win_right;
+  // Block-sparse: 0/1 per (128-query block, 128-key block) pair, [n_qblocks][n_kvtiles] for
+  // every head (bm_per_head = 0) or one such array per (b, h) plane.
+  const uint8_t* block_mask;
+  int bm_per_head, n_qblocks;
 };
 
-template <int D, bool VL, bool F8 = false, bool WIN = false>
+template <int D, bool VL, bool F8 = false, bool WIN = false, bool BS = false>
 __global__ void __launch_bounds__(FwdCfg<D, F8>::THREADS, 1)
 fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D, F8>;
@@ -185,7 +192,7 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
     }
   }
   const int j0 = WIN ? lo[0] : 0;
-  const int n_max = WIN ? ((n_t[1] > 0) ? lo[1] + n_t[1] - j0 : n_t[0]) : max(n_t[0], n_t[1]);
+  int n_max = WIN ? ((n_t[1] > 0) ? lo[1] + n_t[1] - j0 : n_t[0]) : max(n_t[0], n_t[1]);
   off[0] = 0;
   off[1] = lo[1] - j0;
   // TMA coordinates of local row ``row``: fixed length {x, row, (b,h)}; packed {x, h, beg+row}
@@ -214,10 +221,46 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
     tma_prefetch_desc(&p.tv);
     tma_prefetch_desc(&p.to);
   }
+  // Block-sparse: the CTA streams the key tiles either query tile wants (the union of its two
+  // mask rows, in order; with causal only tiles up to the diagonal), once.  Both tiles run
+  // every streamed tile; a tile whose block is not set masks it whole (P = 0).
+  int16_t* s_bsl = reinterpret_cast<int16_t*>(smem + C::OFF_BSL);
+  uint8_t* s_bsb = smem + C::OFF_BSB;
+  if constexpr (BS) {
+    if (warp == 3) {
+      const bool a0 = q0[0] < n_q, a1 = q0[1] < n_q;
+      const int qb0 = q0[0] / C::BM, qb1 = a1 ? q0[1] / C::BM : qb0;
+      const size_t plane = static_cast<size_t>(p.bm_per_head ? bh : 0) * p.n_qblocks;
+      const uint8_t* r0 = p.block_mask + (plane + qb0) * n_kvtiles;
+      const uint8_t* r1 = p.block_mask + (plane + qb1) * n_kvtiles;
+      int cnt = 0;
+      for (int base = 0; base < n_kvtiles; base += 32) {
+        const int kt = base + lane;
+        uint32_t b = 0;
+        if (kt < n_kvtiles) {
+          if (a0 && r0[kt] != 0 && (!p.causal || kt <= qb0)) b |= 1u;
+          if (a1 && r1[kt] != 0 && (!p.causal || kt <= qb1)) b |= 2u;
+        }
+        const uint32_t bal = __ballot_sync(0xffffffffu, b != 0u);
+        if (b != 0u) {
+          const int pos = cnt + __popc(bal & ((1u << lane) - 1u));
+          s_bsl[pos] = static_cast<int16_t>(kt);
+          s_bsb[pos] = static_cast<uint8_t>(b);
+        }
+        cnt += __popc(bal);
+      }
+      if (lane == 0) *reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8) = cnt;
+    }
+  }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  if constexpr (BS) {
+    n_max = *reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) n_t[t] = (q0[t] < n_q) ? n_max : 0;
+  }
   if (warp < 4) {
   setmaxnreg_dec<C::REG_CTRL>();   // warpgroup 0: producer, MMA issuer, two idle warps
   if (warp == 0) {
@@ -232,7 +275,7 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       for (int j = 0; j < n_max; ++j) {               // stream position j = key tile j0 + j
         const int s = j % C::NS;
         const uint32_t u = j / C::NS;
-        const int key = (j0 + j) * C::BN;
+        const int key = (BS ? s_bsl[j] : j0 + j) * C::BN;
         if (u > 0 && !mbar_wait(&k_empty[s], (u - 1) & 1, abort_flag, 101)) break;
         mbar_arrive_expect_tx(&k_full[s], C::TILE);
         for (int k = 0; k < C::KCH; ++k)
@@ -478,9 +521,10 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       }
       tmem_wait_ld();
 
-      const int k0 = (lo_t + j) * C::BN;
+      const int k0 = (BS ? s_bsl[j] : lo_t + j) * C::BN;
       // a tile that some row of the query tile sees only in part (window edge, causal
-      // diagonal, ragged end of the keys) is masked element by element
+      // diagonal, ragged end of the keys) is masked element by element; block-sparse: a
+      // streamed tile this query tile's block is not set for is masked whole
       if constexpr (WIN) {
         if (k0 + C::BN > n_kv || k0 + C::BN - 1 > q0t + min(p.win_right, kWinUnbounded - C::BM) ||
             k0 < q0t + C::BM - 1 - p.win_left) {
@@ -488,8 +532,10 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
           for (int k = 0; k < 128; ++k)
             if (k0 + k < key_lo || k0 + k >= key_hi) s[k] = -INFINITY;
         }
-      } else if (k0 + C::BN > n_kv || (p.causal && k0 + C::BN - 1 > q0t)) {
-        const int lim = p.causal ? min(q_idx + 1, n_kv) : n_kv;   // keys < lim visible
+      } else if (const bool dead = BS && ((s_bsb[j] >> t) & 1u) == 0u;
+                 dead || k0 + C::BN > n_kv || (p.causal && k0 + C::BN - 1 > q0t)) {
+        // keys < lim visible (none of a dead block's)
+        const int lim = dead ? k0 : (p.causal ? min(q_idx + 1, n_kv) : n_kv);
 #pragma unroll
         for (int k = 0; k < 128; ++k)
           if (k0 + k >= lim) s[k] = -INFINITY;
@@ -505,9 +551,9 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       }
       const float mx = fmaxf(fmax3(mq[0], mq[1], mq[2]), mq[3]);
       const float cand = fmaxf(m, mx);
-      // (under a window a row may miss a whole tile: cand = -inf, nothing to move; without
-      // one every row sees a key of its first tile)
-      const bool move = (!WIN || cand != -INFINITY) &&
+      // (under a window or a block mask a row may miss a whole tile: cand = -inf, nothing to
+      // move; otherwise every row sees a key of its first tile)
+      const bool move = (!(WIN || BS) || cand != -INFINITY) &&
                         ((m == -INFINITY) || ((cand - m) * c2 > C::RESCALE_THRESHOLD));
       if (__any_sync(0xffffffffu, move)) {
         const float alpha = move ? fast_exp2((m - cand) * c2) : 1.f;  // 0 when m = -inf
@@ -687,8 +733,18 @@ static cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   p.o = static_cast<uint16_t*>(a.o);
   p.out_scale = 1.f;
   attention_window(a.causal, a.windowed, a.win_left, a.win_right, &p.win_left, &p.win_right);
+  p.block_mask = a.block_mask;
+  p.bm_per_head = a.bm_per_head;
+  p.n_qblocks = (a.n_q + kBlockSize - 1) / kBlockSize;
   static int attr_done[64] = {0};   // one per instantiation of this launcher
   const uint64_t grid = static_cast<uint64_t>(p.n_qpairs) * bh;
+  if (a.block_mask != nullptr) {
+    static int attr_bs[64] = {0};
+    cudaError_t e = ensure_smem_attr(fwd_kernel<D, false, false, false, true>, C::SMEM_BYTES, attr_bs);
+    if (e != cudaSuccess) return e;
+    fwd_kernel<D, false, false, false, true><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError();
+  }
   if (a.windowed) {
     static int attr_win[64] = {0};
     cudaError_t e = ensure_smem_attr(fwd_kernel<D, false, false, true>, C::SMEM_BYTES, attr_win);
@@ -730,6 +786,8 @@ static cudaError_t launch_fwd_varlen_d(const FwdVarlenArgs& a, cudaStream_t stre
   p.o = static_cast<uint16_t*>(a.o);
   p.out_scale = 1.f;
   attention_window(a.causal, false, 0, 0, &p.win_left, &p.win_right);
+  p.block_mask = nullptr;
+  p.bm_per_head = p.n_qblocks = 0;
   static int attr_done[64] = {0};
   cudaError_t e = ensure_smem_attr(fwd_kernel<D, true>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
@@ -766,6 +824,8 @@ cudaError_t launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream) {
   p.o = static_cast<uint16_t*>(a.o);
   p.out_scale = a.descale_v;
   attention_window(a.causal, false, 0, 0, &p.win_left, &p.win_right);
+  p.block_mask = nullptr;
+  p.bm_per_head = p.n_qblocks = 0;
   static int attr_done[64] = {0};
   cudaError_t e = ensure_smem_attr(fwd_kernel<D, false, true>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;

@@ -113,3 +113,19 @@ def make_qkv_fp8(B: int, H: int, N_q: int, N_kv: int, d: int, seed: int, *, devi
         out[name + "8"] = (x / s).to(torch.float8_e4m3fn).view(torch.uint8).contiguous()
         out["descale_" + name] = s
     return out
+
+
+def make_block_mask(n_qblocks: int, n_kblocks: int, seed: int, *, band: int = 1, n_global: int = 1,
+                    p_random: float = 0.05, heads: tuple[int, int] | None = None) -> torch.Tensor:
+    """Seeded 0/1 block pattern (uint8, CPU) of the kind block-sparse attention is used with: a
+    band of ``band`` blocks either side of the diagonal, the first ``n_global`` key blocks for
+    every query block, and each other block with probability ``p_random``.  ``heads = (B, H)``
+    gives one independent pattern per head, [B, H, n_qblocks, n_kblocks]."""
+    gen = torch.Generator().manual_seed(seed)
+    shape = ((*heads, n_qblocks, n_kblocks) if heads else (n_qblocks, n_kblocks))
+    m = torch.rand(shape, generator=gen) < p_random
+    i = torch.arange(n_qblocks)[:, None]
+    j = torch.arange(n_kblocks)[None, :]
+    m |= (j - i).abs() <= band
+    m |= j < n_global
+    return m.to(torch.uint8)

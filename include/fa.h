@@ -85,6 +85,33 @@ fa_status_t fa_bwd_window(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_
                           int window_right, void* stream);
 
 /*
+ * fa_fwd_block_sparse / fa_bwd_block_sparse -- block-sparse attention, forward and backward
+ * ([Scratch] "Results": the method's own block-sparse variant, the same IO-aware tiling applied
+ * to a sparse pattern; the pages fix no pattern, so the pattern is the caller's).
+ *
+ * Blocks are 128 queries x 128 keys.  block_mask is a DEVICE array of bytes, nonzero = the
+ * block is computed: [ceil(N_q/128)][ceil(N_kv/128)] shared by every head (mask_per_head = 0)
+ * or [B*H][ceil(N_q/128)][ceil(N_kv/128)] (mask_per_head = 1), row-major, read during the
+ * call in stream order; the caller owns it.  Query i sees key j iff the block (i/128, j/128)
+ * is set and, with causal (N_q == N_kv), j <= i.  A row that sees no key gets O = 0 and
+ * lse = -inf, and its gradients are 0.  Key blocks no row of a query tile pair sees are never
+ * loaded; the backward visits, for each key block, only the query blocks set with it.
+ * ceil(N_kv/128) <= 1024, else FA_ERR_UNSUPPORTED; mask_per_head not 0/1 or a null mask
+ * (with N_q, N_kv > 0): FA_ERR_INVALID_ARG.  Otherwise exactly fa_fwd / fa_bwd (same layouts,
+ * workspace, errors).
+ */
+fa_status_t fa_fwd_block_sparse(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
+                                fa_bf16_t* o, float* lse, int B, int H, int N_q, int N_kv, int d,
+                                float scale, int causal, const unsigned char* block_mask,
+                                int mask_per_head, void* stream);
+fa_status_t fa_bwd_block_sparse(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
+                                const fa_bf16_t* o, const float* lse, const fa_bf16_t* dO,
+                                fa_bf16_t* dq, fa_bf16_t* dk, fa_bf16_t* dv, void* ws,
+                                size_t ws_bytes, int B, int H, int N_q, int N_kv, int d,
+                                float scale, int causal, const unsigned char* block_mask,
+                                int mask_per_head, void* stream);
+
+/*
  * fa_fwd_fp8 -- attention forward from 8-bit inputs (the low-precision FP8 path [Lesson4]
  * "Causal masks and FlashAttention-3" and [Scratch] "Later versions" name; the pages give no
  * formula, so this follows the plainest reading: one scale per tensor).

@@ -164,3 +164,22 @@ def test_window_entry_points_validate_like_the_plain_ones(lib):
     args = [FAKE] * 9
     st = lib.fa_bwd_window(*args, FAKE, need - 1, 1, 2, 256, 128, 0.1, 10, 0, None)
     assert st == WORKSPACE
+
+
+def test_block_sparse_entry_points_validate_before_launching(lib):
+    fwd = lib.fa_fwd_block_sparse
+    # (q, k, v, o, lse, B, H, N_q, N_kv, d, scale, causal, mask, per_head, stream)
+    assert fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 256, 256, 96, 0.1, 0, FAKE, 0, None) == UNSUPPORTED
+    assert fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 256, 256, 128, 0.1, 0, None, 0, None) == INVALID
+    assert fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 256, 256, 128, 0.1, 0, FAKE, 2, None) == INVALID
+    assert fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 256, 384, 128, 0.1, 1, FAKE, 0, None) == UNSUPPORTED
+    # more than 1024 key blocks
+    assert fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, 128, 1024 * 128 + 1, 128, 0.1, 0, FAKE, 0,
+               None) == UNSUPPORTED
+    assert fwd(FAKE, FAKE, FAKE, FAKE, FAKE, 1, 2, 256, 256, 128, float("nan"), 0, FAKE, 0, None) == INVALID
+    need = lib.fa_bwd_workspace_size(1, 2, 256, 256, 128)
+    args = [FAKE] * 9
+    bwd = lib.fa_bwd_block_sparse
+    assert bwd(*args, FAKE, need - 1, 1, 2, 256, 256, 128, 0.1, 0, FAKE, 0, None) == WORKSPACE
+    assert bwd(*args, FAKE, need, 1, 2, 256, 256, 128, 0.1, 0, None, 0, None) == INVALID
+    assert bwd(*args, FAKE, need, 1, 2, 256, 256, 64, 0.1, 1, FAKE, 3, None) == INVALID

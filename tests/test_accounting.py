@@ -44,3 +44,23 @@ def test_window_pairs_special_cases_and_brute_force():
         if r >= 0:
             vis &= j <= i + r
         assert W.window_pairs(n, l, r) == int(vis.sum())
+
+
+def test_block_sparse_pairs_brute_force():
+    import numpy as np
+    g = np.random.default_rng(2)
+    for n_q, n_kv, causal, block in ((37, 37, True, 4), (37, 29, False, 4), (300, 300, True, 128),
+                                     (64, 64, False, 16)):
+        nqb, nkb = -(-n_q // block), -(-n_kv // block)
+        m = (g.random((2, 3, nqb, nkb)) < 0.5).astype(np.uint8)
+        brute = 0
+        for h in m.reshape(-1, nqb, nkb):
+            i = np.arange(n_q)[:, None]
+            j = np.arange(n_kv)[None, :]
+            vis = h.astype(bool)[i // block, j // block]
+            if causal:
+                vis &= j <= i
+            brute += int(vis.sum())
+        assert W.block_sparse_pairs(m, n_q, n_kv, causal, block) == brute
+    assert W.block_sparse_pairs(np.ones((3, 3)), 300, 300, True) == W.pairs(300, 300, True)
+    assert W.block_sparse_pairs(np.ones((3, 3)), 300, 300, False) == W.pairs(300, 300, False)
