@@ -67,9 +67,10 @@ struct FwdCfg {
   static constexpr int OFF_BAR = F8 ? OFF_OST + 2 * OTILE : OFF_V + NS * TILE;
   // q_full, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[2], p_full[2], o_done[2]
   static constexpr int NBAR = 1 + 4 * NS + 6;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;      // TMEM slot, abort flag, list length
+  // TMEM slot, abort flag, block-sparse stream length and live counts of the two query tiles
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   // block-sparse: the CTA's key-tile stream (int16 indices) and which query tile wants each
-  static constexpr int OFF_BSL = OFF_MISC + 16;
+  static constexpr int OFF_BSL = OFF_MISC + 32;
   static constexpr int OFF_BSB = OFF_BSL + 2 * kBlockSparseMaxTiles;
   static constexpr int SMEM_BYTES = OFF_BSB + kBlockSparseMaxTiles + 1024;   // + 1 KB alignment slack
   static constexpr uint32_t TMEM_COLS = 512;
@@ -233,7 +234,7 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       const size_t plane = static_cast<size_t>(p.bm_per_head ? bh : 0) * p.n_qblocks;
       const uint8_t* r0 = p.block_mask + (plane + qb0) * n_kvtiles;
       const uint8_t* r1 = p.block_mask + (plane + qb1) * n_kvtiles;
-      int cnt = 0;
+      int cnt = 0, live0 = 0, live1 = 0;
       for (int base = 0; base < n_kvtiles; base += 32) {
         const int kt = base + lane;
         uint32_t b = 0;
@@ -241,6 +242,8 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
           if (a0 && r0[kt] != 0 && (!p.causal || kt <= qb0)) b |= 1u;
           if (a1 && r1[kt] != 0 && (!p.causal || kt <= qb1)) b |= 2u;
         }
+        live0 += __popc(__ballot_sync(0xffffffffu, (b & 1u) != 0u));
+        live1 += __popc(__ballot_sync(0xffffffffu, (b & 2u) != 0u));
         const uint32_t bal = __ballot_sync(0xffffffffu, b != 0u);
         if (b != 0u) {
           const int pos = cnt + __popc(bal & ((1u << lane) - 1u));
@@ -249,17 +252,26 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
         }
         cnt += __popc(bal);
       }
-      if (lane == 0) *reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8) = cnt;
+      if (lane == 0) {
+        volatile int* nb = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
+        nb[0] = cnt;
+        nb[1] = live0;                             // live blocks of each query tile
+        nb[2] = live1;
+      }
     }
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  // block-sparse: n_max stream positions; tile t runs only its n_t[t] live ones (a clear block
+  // is neither computed nor waited for)
+  auto live = [&](int t, int j) { return ((s_bsb[j] >> t) & 1u) != 0u; };
   if constexpr (BS) {
-    n_max = *reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
-#pragma unroll
-    for (int t = 0; t < 2; ++t) n_t[t] = (q0[t] < n_q) ? n_max : 0;
+    const volatile int* nb = reinterpret_cast<const volatile int*>(smem + C::OFF_MISC + 8);
+    n_max = nb[0];
+    n_t[0] = nb[1];
+    n_t[1] = nb[2];
   }
   if (warp < 4) {
   setmaxnreg_dec<C::REG_CTRL>();   // warpgroup 0: producer, MMA issuer, two idle warps
@@ -267,11 +279,13 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0 && n_max > 0) {
       int issued = 0;
-      const int nq_tiles = (n_t[1] > 0) ? 2 : 1;
-      mbar_arrive_expect_tx(q_full, nq_tiles * C::TILE);
-      for (int t = 0; t < nq_tiles; ++t)
-        for (int k = 0; k < C::KCH; ++k)
-          tma_load_3d(sQ + t * C::TILE + k * C::CHUNK, &p.tq, q_full, k * C::XCH, y1(q0[t]), y2(q_beg, q0[t]));
+      // Q_t only for a tile with work: a tile without any (block-sparse: no set block) writes
+      // its O = 0 through the staging area at once, which for bf16 is its Q buffer
+      mbar_arrive_expect_tx(q_full, ((n_t[0] > 0) + (n_t[1] > 0)) * C::TILE);
+      for (int t = 0; t < 2; ++t)
+        if (n_t[t] > 0)
+          for (int k = 0; k < C::KCH; ++k)
+            tma_load_3d(sQ + t * C::TILE + k * C::CHUNK, &p.tq, q_full, k * C::XCH, y1(q0[t]), y2(q_beg, q0[t]));
       for (int j = 0; j < n_max; ++j) {               // stream position j = key tile j0 + j
         const int s = j % C::NS;
         const uint32_t u = j / C::NS;
@@ -432,14 +446,51 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
         }
       };
       bool ok = mbar_wait(q_full, 0, abort_flag, 111) && mbar_wait(&k_full[0], 0, abort_flag, 112);
-      if (ok) {
+      if constexpr (BS) {
+        // Only live (tile, block) pairs are computed; cnt[t] counts tile t's live steps.  An
+        // S_t(j+1) of a tile that is clear at j waits for the other tile's hand-off at j, which
+        // vouches for K_{j+1} (the helper checked it).
+        int cnt[2] = {0, 0};
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            if (live(t, 0)) issue_s(t, 0);
+          umma_commit(&k_empty[0]);
+        }
+        for (int j = 0; ok && j < n_max; ++j) {
+          const int s = j % C::NS;
+          const bool nxt = j + 1 < n_max;
+          bool waited = false;
+          int deferred = -1;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (live(t, j)) {
+              if (!(ok = mbar_wait(&p_full[t], cnt[t] & 1, abort_flag, 115 + t))) break;
+              tc_fence_after();
+              waited = true;
+              issue_pv(t, j, cnt[t] == 0);
+              if (++cnt[t] == n_t[t]) umma_commit(&o_done[t]);
+            }
+            if (nxt && live(t, j + 1)) {
+              if (waited) issue_s(t, j + 1);
+              else deferred = t;
+            }
+          }
+          if (!ok) break;
+          if (deferred >= 0) issue_s(deferred, j + 1);
+          umma_commit(&v_empty[s]);
+          if (nxt) umma_commit(&k_empty[(j + 1) % C::NS]);
+        }
+      }
+      if (!BS && ok) {
         tc_fence_after();
         if (n_t[0] > 0) issue_s(0, 0);
         if (n_t[1] > 0 && (!WIN || off[1] == 0)) issue_s(1, 0);
         umma_commit(&k_empty[0]);
       }
       // stream position j; tile t is on its i-th key tile, i = j - off[t]
-      for (int j = 0; ok && j < n_max; ++j) {
+      for (int j = 0; !BS && ok && j < n_max; ++j) {
         const int s = j % C::NS;
         // V_j and K_{j+1} are loaded: the helper checked them before its p_full arrival
 #pragma unroll
@@ -462,11 +513,12 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
     // ------------------------------------------------------------------ helper
     if (lane == 0 && n_max > 0) {
       bool ok = true;
+      int cnt[2] = {0, 0};                           // block-sparse: live steps per tile
       for (int j = 0; ok && j < n_max; ++j) {
         if (!(ok = mbar_wait(&v_full[j % C::NS], (j / C::NS) & 1, abort_flag, 130))) break;
-        bool k_next = false;                         // does some tile need S(j+1)?
+        bool k_next = BS && j + 1 < n_max;           // does some tile need S(j+1)?
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
+        for (int t = 0; t < 2 && !BS; ++t) {
           const int i = WIN ? j - off[t] : j;
           k_next |= (!WIN || i + 1 >= 0) && i + 1 < n_t[t];
         }
@@ -474,8 +526,9 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
           break;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          const int i = WIN ? j - off[t] : j;
-          if ((!WIN || i >= 0) && i < n_t[t]) {
+          const int i = BS ? cnt[t] : (WIN ? j - off[t] : j);
+          if (BS ? live(t, j) : ((!WIN || i >= 0) && i < n_t[t])) {
+            if constexpr (BS) ++cnt[t];
             // arrive on phase i only once phase i-1 is complete
             if (i > 0 && !(ok = mbar_wait(&p_full[t], (i - 1) & 1, abort_flag, 132 + t))) break;
             mbar_arrive(&p_full[t]);
@@ -508,7 +561,13 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
     bool ok = true;
     int handed = 0;                           // fp8: P hand-offs joined so far
 
+    int pos = 0;                              // block-sparse: stream position of step j
     for (int j = 0; j < n; ++j) {
+      int jp = j;
+      if constexpr (BS) {                       // next stream position this tile's block is set at
+        while (pos < n_max - 1 && !live(t, pos)) ++pos;
+        jp = pos++;
+      }
       if (!(ok = mbar_wait_warp(&s_full[t], j & 1, abort_flag, 121))) break;
       tc_fence_after();
       float s[128];
@@ -521,10 +580,9 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       }
       tmem_wait_ld();
 
-      const int k0 = (BS ? s_bsl[j] : lo_t + j) * C::BN;
+      const int k0 = (BS ? s_bsl[jp] : lo_t + j) * C::BN;
       // a tile that some row of the query tile sees only in part (window edge, causal
-      // diagonal, ragged end of the keys) is masked element by element; block-sparse: a
-      // streamed tile this query tile's block is not set for is masked whole
+      // diagonal, ragged end of the keys) is masked element by element
       if constexpr (WIN) {
         if (k0 + C::BN > n_kv || k0 + C::BN - 1 > q0t + min(p.win_right, kWinUnbounded - C::BM) ||
             k0 < q0t + C::BM - 1 - p.win_left) {
@@ -532,10 +590,8 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
           for (int k = 0; k < 128; ++k)
             if (k0 + k < key_lo || k0 + k >= key_hi) s[k] = -INFINITY;
         }
-      } else if (const bool dead = BS && ((s_bsb[j] >> t) & 1u) == 0u;
-                 dead || k0 + C::BN > n_kv || (p.causal && k0 + C::BN - 1 > q0t)) {
-        // keys < lim visible (none of a dead block's)
-        const int lim = dead ? k0 : (p.causal ? min(q_idx + 1, n_kv) : n_kv);
+      } else if (k0 + C::BN > n_kv || (p.causal && k0 + C::BN - 1 > q0t)) {
+        const int lim = p.causal ? min(q_idx + 1, n_kv) : n_kv;   // keys < lim visible
 #pragma unroll
         for (int k = 0; k < 128; ++k)
           if (k0 + k >= lim) s[k] = -INFINITY;
