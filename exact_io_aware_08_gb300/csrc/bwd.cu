@@ -66,8 +66,10 @@ struct BwdCfg {
   // kv_full, stage_full[NST], stage_empty[NST], st_full, dp_full, p_ready, ds_ready,
   // pds_free[2], dq_full[2], dq_free[2], mma_done, dqs_sync
   static constexpr int NBAR = 1 + 2 * NST + 12;
-  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;       // TMEM slot, abort flag, step count
+  // block-sparse: one bit per query block, set where this CTA's key tile has work
+  static constexpr int OFF_BSW = OFF_MISC + 16;
+  static constexpr int SMEM_BYTES = OFF_BSW + kBlockSparseMaxTiles / 8 + 1024;
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t T_DV = 0;
   static constexpr uint32_t T_DK = D;
@@ -183,12 +185,18 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
     return bs_col[static_cast<size_t>(qb) * p.n_kvtiles] != 0 && (!p.causal || qb >= kt);
   };
   auto bs_steps = [&](int qb) { return min(kBlockSize / C::BM, (n_q - qb * kBlockSize + C::BM - 1) / C::BM); };
+  const uint32_t* s_bsw = reinterpret_cast<const uint32_t*>(smem + C::OFF_BSW);
+  const int bs_words = (p.n_qblocks + 31) / 32;
   int bs_qb = -1, bs_sub = 0;
   auto step_q0 = [&](int i) -> int {
     if constexpr (BS) {
       if (bs_qb < 0 || ++bs_sub >= bs_steps(bs_qb)) {
-        bs_sub = 0;
-        do { ++bs_qb; } while (bs_qb < p.n_qblocks && !bs_set(bs_qb));
+        bs_sub = 0;                             // next set query block, from the bit words
+        const int q = bs_qb + 1;
+        int w = q >> 5;
+        uint32_t word = (w < bs_words) ? (s_bsw[w] & (0xffffffffu << (q & 31))) : 0u;
+        while (word == 0u && ++w < bs_words) word = s_bsw[w];
+        bs_qb = (word != 0u) ? (w << 5) + __ffs(word) - 1 : p.n_qblocks;
       }
       return bs_qb * kBlockSize + bs_sub * C::BM;
     } else {
@@ -197,10 +205,14 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
   };
   if constexpr (BS) {
     if (warp == 14) {
+      uint32_t* w_out = reinterpret_cast<uint32_t*>(smem + C::OFF_BSW);
       int cnt = 0;
       for (int base = 0; base < p.n_qblocks; base += 32) {
         const int qb = base + lane;
-        cnt += __reduce_add_sync(0xffffffffu, (qb < p.n_qblocks && bs_set(qb)) ? bs_steps(qb) : 0);
+        const bool set = qb < p.n_qblocks && bs_set(qb);
+        const uint32_t bal = __ballot_sync(0xffffffffu, set);
+        if (lane == 0) w_out[base >> 5] = bal;
+        cnt += __reduce_add_sync(0xffffffffu, set ? bs_steps(qb) : 0);
       }
       if (lane == 0) *reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8) = cnt;
     }
