@@ -118,6 +118,7 @@ struct FwdParams {
   // every head (bm_per_head = 0) or one such array per (b, h) plane.
   const uint8_t* block_mask;
   int bm_per_head, n_qblocks;
+  int n_items;                                        // persistent forward: B*H*n_qpairs
 };
 
 template <int D, bool VL, bool F8 = false, bool WIN = false, bool BS = false>
@@ -762,6 +763,416 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
   }
 }
 
+// ------------------------------------------------------------------------------------------
+// Persistent forward (plain bf16: no window, block mask, varlen or fp8).  One CTA per SM walks
+// the work items blockIdx.x, blockIdx.x + gridDim.x, ... (the same items, in the same
+// longest-first order, as one CTA per item), so that one item's tail overlaps the next one's
+// start: the next item's Q is loaded as soon as the current item's last S products complete,
+// its first S products follow the last PV products, and the softmax warps store the finished
+// item's O (through a staging buffer the two tiles take in turn) while the tensor core works.
+// Every mbarrier phase is counted across items.  Roles, TMEM and the online softmax are those
+// of fwd_kernel.
+// ------------------------------------------------------------------------------------------
+// Heads of at most this many key tiles run on the persistent forward.
+constexpr int kPersistentMaxKvTiles = 8;
+
+template <int D>
+struct FwdPCfg {
+  static constexpr int BM = 128, BN = 128;
+  static constexpr int KCH = D * 2 / 128;             // 128-byte chunks per bf16 row
+  static constexpr int TILE = 128 * D * 2;            // one 128-row Q/K/V tile (bf16)
+  static constexpr int CHUNK = 128 * 128;
+  static constexpr int OCH = D / 64;
+  static constexpr int NS = (D == 128) ? 2 : 4;
+  static constexpr int KS_S = D / 16, KS_PV = BN / 16;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = 2 * TILE;
+  static constexpr int OFF_V = OFF_K + NS * TILE;
+  static constexpr int OFF_OST = OFF_V + NS * TILE;   // one O tile of staging, the tiles in turn
+  static constexpr int OFF_BAR = OFF_OST + TILE;
+  // q_full, q_empty, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[2], p_full[2],
+  // o_done[2], o_free[2], st_free
+  static constexpr int NBAR = 2 + 4 * NS + 9;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr uint32_t TMEM_COLS = 512, T_S = 0, T_O = 256;
+  static constexpr int THREADS = 384;
+  static constexpr uint32_t REG_CTRL = 80, REG_SOFTMAX = 208;
+  static constexpr float RESCALE_THRESHOLD = 8.f;
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget (227 KB per CTA)");
+};
+
+// One work item of the fixed-length forward: query rows [256 c, 256 c + 256) of plane bh, and
+// the key tiles each of its two query tiles streams.
+struct FwdItem {
+  int bh, q0[2], n_t[2], n_max;
+};
+
+__device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int item) {
+  FwdItem it;
+  int bh = item / p.n_qpairs, r = item % p.n_qpairs;
+  if (p.causal) causal_item(item, p.n_items / p.n_qpairs, p.n_qpairs, &bh, &r);
+  const int c = p.causal ? (p.n_qpairs - 1 - r) : r;
+  it.bh = bh;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    it.q0[t] = c * 256 + t * 128;
+    it.n_t[t] = (it.q0[t] >= p.n_q) ? 0 : (p.causal ? min(2 * c + t + 1, p.n_kvtiles) : p.n_kvtiles);
+  }
+  it.n_max = max(it.n_t[0], it.n_t[1]);
+  return it;
+}
+
+template <int D>
+__global__ void __launch_bounds__(FwdPCfg<D>::THREADS, 1)
+fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
+  using C = FwdPCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_smem_1k(smem_raw);
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sK = smem + C::OFF_K;
+  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sO = smem + C::OFF_OST;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;
+  uint64_t* k_empty = k_full + C::NS;
+  uint64_t* v_full = k_empty + C::NS;
+  uint64_t* v_empty = v_full + C::NS;
+  uint64_t* s_full = v_empty + C::NS;      // [2]
+  uint64_t* p_full = s_full + 2;           // [2]
+  uint64_t* o_done = p_full + 2;           // [2]
+  uint64_t* o_free = o_done + 2;           // [2]: the tile's O read out of TMEM by its epilogue
+  uint64_t* st_free = o_free + 2;          // the O staging buffer is free again
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = gridDim.x;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&s_full[t], 1);
+      mbar_init(&p_full[t], 129);         // the tile's 128 softmax threads + the helper
+      mbar_init(&o_done[t], 1);
+      mbar_init(&o_free[t], 128);
+    }
+    mbar_init(st_free, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tq);
+    tma_prefetch_desc(&p.tk);
+    tma_prefetch_desc(&p.tv);
+    tma_prefetch_desc(&p.to);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp < 4) {
+  setmaxnreg_dec<C::REG_CTRL>();
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t P = 0, issued = 0;             // stream positions over all items
+      int nq = 0;                             // Q loads issued
+      bool ok = true;
+      for (int k = 0; ok && blockIdx.x + k * G < p.n_items; ++k) {
+        const FwdItem it = fwd_item(p, blockIdx.x + k * G);
+        if (k > 0 && !(ok = mbar_wait(q_empty, (k - 1) & 1, abort_flag, 141))) break;
+        mbar_arrive_expect_tx(q_full, ((it.n_t[0] > 0) + (it.n_t[1] > 0)) * C::TILE);
+        for (int t = 0; t < 2; ++t)
+          if (it.n_t[t] > 0)
+            for (int c = 0; c < C::KCH; ++c)
+              tma_load_3d(sQ + t * C::TILE + c * C::CHUNK, &p.tq, q_full, c * 64, it.q0[t], it.bh);
+        nq = k + 1;
+        for (int j = 0; j < it.n_max; ++j, ++P) {
+          const int s = P % C::NS;
+          const uint32_t u = P / C::NS;
+          const int key = j * C::BN;
+          if (u > 0 && !(ok = mbar_wait(&k_empty[s], (u - 1) & 1, abort_flag, 142))) break;
+          mbar_arrive_expect_tx(&k_full[s], C::TILE);
+          for (int c = 0; c < C::KCH; ++c)
+            tma_load_3d(sK + s * C::TILE + c * C::CHUNK, &p.tk, &k_full[s], c * 64, key, it.bh);
+          if (u > 0 && !(ok = mbar_wait(&v_empty[s], (u - 1) & 1, abort_flag, 143))) break;
+          mbar_arrive_expect_tx(&v_full[s], C::TILE);
+          for (int c = 0; c < C::KCH; ++c)
+            tma_load_3d(sV + s * C::TILE + c * C::CHUNK, &p.tv, &v_full[s], c * 64, key, it.bh);
+          issued = P + 1;
+        }
+      }
+      if (*abort_flag) {
+        // let every copy this thread started land before the CTA exits
+        if (nq > 0) mbar_wait(q_full, (nq - 1) & 1, nullptr, 144);
+        for (uint32_t q = issued > C::NS ? issued - C::NS : 0; q < issued; ++q) {
+          mbar_wait(&k_full[q % C::NS], (q / C::NS) & 1, nullptr, 145);
+          mbar_wait(&v_full[q % C::NS], (q / C::NS) & 1, nullptr, 146);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
+      const uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
+      const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 0, 1024);
+      const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 0, 1024);
+      const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), C::CHUNK, 1024);
+      auto issue_s = [&](int t, uint32_t P) {                  // S_t = Q_t K^T (position P)
+        const uint64_t a = desc_advance(dq0, t * C::TILE);
+        const uint64_t b = desc_advance(dk0, (P % C::NS) * C::TILE);
+#pragma unroll
+        for (int ks = 0; ks < C::KS_S; ++ks) {
+          const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
+          umma_ss(tbase + C::T_S + t * 128, desc_advance(a, off), desc_advance(b, off), idesc_s, ks > 0);
+        }
+        umma_commit(&s_full[t]);
+      };
+      auto issue_pv = [&](int t, uint32_t P, bool first) {     // O_t += P_t V (position P)
+        const uint64_t b = desc_advance(dv0, (P % C::NS) * C::TILE);
+#pragma unroll
+        for (int ks = 0; ks < C::KS_PV; ++ks)
+          umma_ts(tbase + C::T_O + t * D, tbase + C::T_S + t * 128 + ks * 8,
+                  desc_advance(b, ks * 16 * 128), idesc_o, (!first || ks > 0) ? 1u : 0u);
+      };
+      uint32_t P = 0, cp[2] = {0, 0}, act[2] = {0, 0};
+      bool ok = true;
+      for (int k = 0; ok && blockIdx.x + k * G < p.n_items; ++k) {
+        const FwdItem it = fwd_item(p, blockIdx.x + k * G);
+        if (!(ok = mbar_wait(q_full, k & 1, abort_flag, 151) &&
+                   mbar_wait(&k_full[P % C::NS], (P / C::NS) & 1, abort_flag, 152)))
+          break;
+        tc_fence_after();
+        // the S columns are free: the previous item's last PV products were issued before
+        for (int t = 0; t < 2; ++t)
+          if (it.n_t[t] > 0) issue_s(t, P);
+        umma_commit(&k_empty[P % C::NS]);
+        if (it.n_max == 1) umma_commit(q_empty);
+        for (int j = 0; ok && j < it.n_max; ++j) {
+          const uint32_t Pj = P + j;
+          // V_j and K_{j+1} are loaded: the helper checked them before its p_full arrival
+          for (int t = 0; t < 2; ++t) {
+            if (j < it.n_t[t]) {
+              if (!(ok = mbar_wait(&p_full[t], cp[t] & 1, abort_flag, 153 + t))) break;
+              ++cp[t];
+              // O_t of this tile's previous item has been read out by its epilogue
+              if (j == 0 && act[t] > 0 && !(ok = mbar_wait(&o_free[t], (act[t] - 1) & 1, abort_flag, 155 + t)))
+                break;
+              tc_fence_after();
+              issue_pv(t, Pj, j == 0);
+              if (j + 1 == it.n_t[t]) umma_commit(&o_done[t]);
+            }
+            if (j + 1 < it.n_t[t]) issue_s(t, Pj + 1);
+          }
+          if (!ok) break;
+          umma_commit(&v_empty[Pj % C::NS]);
+          if (j + 1 < it.n_max) umma_commit(&k_empty[(Pj + 1) % C::NS]);
+          if (j + 2 == it.n_max) umma_commit(q_empty);     // the item's last S products issued
+        }
+        for (int t = 0; t < 2; ++t) act[t] += it.n_t[t] > 0;
+        P += it.n_max;
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------------ helper
+    // Folds "V_j loaded" and "K_{j+1} loaded" into each P hand-off (the MMA thread waits once
+    // per hand-off); arrives on phase i of a tile's p_full only once phase i-1 is complete.
+    if (lane == 0) {
+      uint32_t P = 0, ch[2] = {0, 0};
+      bool ok = true;
+      for (int k = 0; ok && blockIdx.x + k * G < p.n_items; ++k) {
+        const FwdItem it = fwd_item(p, blockIdx.x + k * G);
+        for (int j = 0; ok && j < it.n_max; ++j) {
+          const uint32_t Pj = P + j;
+          if (!(ok = mbar_wait(&v_full[Pj % C::NS], (Pj / C::NS) & 1, abort_flag, 161))) break;
+          if (j + 1 < it.n_max &&
+              !(ok = mbar_wait(&k_full[(Pj + 1) % C::NS], ((Pj + 1) / C::NS) & 1, abort_flag, 162)))
+            break;
+          for (int t = 0; t < 2; ++t) {
+            if (j < it.n_t[t]) {
+              if (ch[t] > 0 && !(ok = mbar_wait(&p_full[t], (ch[t] - 1) & 1, abort_flag, 163 + t))) break;
+              mbar_arrive(&p_full[t]);
+              ++ch[t];
+            }
+          }
+        }
+        P += it.n_max;
+      }
+    }
+  }
+  } else {
+  setmaxnreg_inc<C::REG_SOFTMAX>();
+{
+    // ------------------------------------------------------------------ softmax warpgroups
+    const int t = (warp - 4) >> 2;
+    const int sub = warp & 3;
+    const int row = sub * 32 + lane;
+    const uint32_t t_lane = static_cast<uint32_t>(sub * 32) << 16;
+    const uint32_t t_s = tbase + t_lane + C::T_S + t * 128;
+    const uint32_t t_o = tbase + t_lane + C::T_O + t * D;
+    const float c2 = p.scale_log2;
+    const float2 c2v = make_float2(c2, c2);
+    uint32_t cs = 0, act = 0, uses = 0;       // S hand-offs, items of this tile, staging uses
+    bool ok = true;
+    for (int k = 0; ok && blockIdx.x + k * G < p.n_items; ++k) {
+      const FwdItem it = fwd_item(p, blockIdx.x + k * G);
+      // the staging buffer goes to the items' active tiles in order: tile 0, then tile 1
+      const uint32_t my_use = uses + ((t == 1 && it.n_t[0] > 0) ? 1u : 0u);
+      uses += (it.n_t[0] > 0) + (it.n_t[1] > 0);
+      const int n = it.n_t[t];
+      if (n == 0) continue;
+      const int q0t = it.q0[t];
+      const int q_idx = q0t + row;
+      float m = -INFINITY, l = 0.f, lb = 0.f;
+      for (int j = 0; j < n; ++j) {
+        if (!(ok = mbar_wait_warp(&s_full[t], cs & 1, abort_flag, 171))) break;
+        ++cs;
+        tc_fence_after();
+        float s[128];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          uint32_t rr[32];
+          tmem_ld32(t_s + kk * 32, rr);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[kk * 32 + i] = __uint_as_float(rr[i]);
+        }
+        tmem_wait_ld();
+        const int k0 = j * C::BN;
+        if (k0 + C::BN > p.n_kv || (p.causal && k0 + C::BN - 1 > q0t)) {
+          const int lim = p.causal ? min(q_idx + 1, p.n_kv) : p.n_kv;   // keys < lim visible
+#pragma unroll
+          for (int kk = 0; kk < 128; ++kk)
+            if (k0 + kk >= lim) s[kk] = -INFINITY;
+        }
+        float mq[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          mq[g] = fmax3(s[32 * g], s[32 * g + 1], s[32 * g + 2]);
+#pragma unroll
+          for (int kk = 3; kk < 31; kk += 2) mq[g] = fmax3(mq[g], s[32 * g + kk], s[32 * g + kk + 1]);
+          mq[g] = fmaxf(mq[g], s[32 * g + 31]);
+        }
+        const float cand = fmaxf(m, fmaxf(fmax3(mq[0], mq[1], mq[2]), mq[3]));
+        // every row sees a key of its first tile, so cand is finite from there on
+        const bool move = (m == -INFINITY) || ((cand - m) * c2 > C::RESCALE_THRESHOLD);
+        if (__any_sync(0xffffffffu, move)) {
+          const float alpha = move ? fast_exp2((m - cand) * c2) : 1.f;
+          if (move) {
+            l *= alpha;
+            lb *= alpha;
+            m = cand;
+          }
+          if (j > 0) {                          // O_t settled: PV_t(j-1) preceded S_t(j)
+#pragma unroll
+            for (int kk = 0; kk < D / 32; ++kk) {
+              uint32_t rr[32];
+              tmem_ld32(t_o + kk * 32, rr);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                const float2 v = fmul2(make_float2(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1])),
+                                       make_float2(alpha, alpha));
+                rr[i] = __float_as_uint(v.x);
+                rr[i + 1] = __float_as_uint(v.y);
+              }
+              tmem_st32(t_o + kk * 32, rr);
+            }
+          }
+        }
+        const float2 nms = make_float2(-m * c2, -m * c2);
+        float2 rs[4], rb[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) rs[g] = rb[g] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {           // P (bf16) over the first 64 columns of S_t
+          uint32_t pk[32];
+#pragma unroll
+          for (int kk = 0; kk < 32; ++kk) {
+            const float2 x = ffma2(make_float2(s[64 * h + 2 * kk], s[64 * h + 2 * kk + 1]), c2v, nms);
+            const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+            pk[kk] = pack_bf16x2(p0, p1);
+            rs[kk & 3] = fadd2(rs[kk & 3], make_float2(p0, p1));
+            // lb sums the bf16 weights the PV product uses (O / lb is their exact average)
+            rb[kk & 3] = fadd2(rb[kk & 3], make_float2(__uint_as_float(pk[kk] << 16),
+                                                       __uint_as_float(pk[kk] & 0xffff0000u)));
+          }
+          tmem_st32(t_s + h * 32, pk);
+        }
+        const float2 rs01 = fadd2(fadd2(rs[0], rs[1]), fadd2(rs[2], rs[3]));
+        const float2 rb01 = fadd2(fadd2(rb[0], rb[1]), fadd2(rb[2], rb[3]));
+        l += rs01.x + rs01.y;
+        lb += rb01.x + rb01.y;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&p_full[t]);
+      }
+      // ---------------------------------------------------------------- epilogue of the item
+      // Every warp of the group reaches the group barrier below once per item, whatever its
+      // waits returned (a named barrier cannot time out); the barrier ORs the failures, and the
+      // whole group leaves together.
+      if (ok) ok = mbar_wait_warp(&o_done[t], act & 1, abort_flag, 172);
+      ++act;
+      if (ok && my_use > 0) ok = mbar_wait_warp(st_free, (my_use - 1) & 1, abort_flag, 173);
+      if (ok) {
+        tc_fence_after();
+        const float inv_l = (lb > 0.f) ? 1.f / lb : 0.f;
+#pragma unroll
+        for (int kk = 0; kk < D / 32; ++kk) {
+          uint32_t rr[32];
+          tmem_ld32(t_o + kk * 32, rr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 v4;
+            v4.x = pack_bf16x2(__uint_as_float(rr[i + 0]) * inv_l, __uint_as_float(rr[i + 1]) * inv_l);
+            v4.y = pack_bf16x2(__uint_as_float(rr[i + 2]) * inv_l, __uint_as_float(rr[i + 3]) * inv_l);
+            v4.z = pack_bf16x2(__uint_as_float(rr[i + 4]) * inv_l, __uint_as_float(rr[i + 5]) * inv_l);
+            v4.w = pack_bf16x2(__uint_as_float(rr[i + 6]) * inv_l, __uint_as_float(rr[i + 7]) * inv_l);
+            const int col = kk * 32 + i;
+            *reinterpret_cast<uint4*>(sO + (col >> 6) * C::CHUNK + sw128_offset(row, col & 63)) = v4;
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&o_free[t]);                // the next item's first PV may overwrite O_t
+      }
+      if (ok && q_idx < p.n_q)
+        p.lse[static_cast<size_t>(it.bh) * p.n_q + q_idx] = (l > 0.f) ? fmaf(m, p.scale, logf(l)) : -INFINITY;
+      fence_proxy_async_smem();
+      if (named_bar_red_or(1 + t, 128, !ok)) {
+        ok = false;
+        break;
+      }
+      if ((threadIdx.x & 127) == 64) {
+        for (int c = 0; c < C::OCH; ++c) tma_store_3d(&p.to, sO + c * C::CHUNK, c * 64, q0t, it.bh);
+        bulk_commit_group();
+        bulk_wait_group_read0();              // the staging buffer may be reused
+        mbar_arrive(st_free);
+      }
+    }
+  }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+}
+
 template <int D>
 static cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   using C = FwdCfg<D>;
@@ -799,6 +1210,22 @@ static cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
     cudaError_t e = ensure_smem_attr(fwd_kernel<D, false, false, false, true>, C::SMEM_BYTES, attr_bs);
     if (e != cudaSuccess) return e;
     fwd_kernel<D, false, false, false, true><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError();
+  }
+  if (!a.windowed && a.n_kv > 0 && p.n_kvtiles <= kPersistentMaxKvTiles) {
+    // short items: the persistent kernel, one CTA per SM over the same items (measured: the
+    // overlap at item boundaries pays when an item streams few key tiles; with long items the
+    // one-CTA-per-item kernel runs its steps faster and wins)
+    using PC = FwdPCfg<D>;
+    static int attr_p[64] = {0};
+    cudaError_t e = ensure_smem_attr(fwd_persistent_kernel<D>, PC::SMEM_BYTES, attr_p);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    p.n_items = static_cast<int>(grid);
+    const unsigned ctas = static_cast<unsigned>(std::min<uint64_t>(grid, static_cast<uint64_t>(std::max(sms, 1))));
+    fwd_persistent_kernel<D><<<ctas, PC::THREADS, PC::SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
   }
   if (a.windowed) {

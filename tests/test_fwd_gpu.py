@@ -129,3 +129,28 @@ def test_fwd_respects_stream():
     s.synchronize()
     o_ref, lse_ref = A.forward(x["q"], x["k"], x["v"], 0.125, False)
     assert_o_close(o, o_ref)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("d", [64, 128])
+def test_fwd_short_heads_many_items_per_cta(causal, d):
+    """Heads of at most 8 key tiles run on the persistent forward, each CTA taking several work
+    items (here 4 x 32 heads x 2 query pairs = 256 items): it must agree bit for bit with the
+    one-CTA-per-item kernel, which the windowed entry point runs for the same mask, and with the
+    oracle on sampled heads."""
+    require_gpu()
+    B, H, N = 4, 32, 1000
+    x = inputs.make_qkv(B, H, N, N, d, seed=77 + d, with_do=False)
+    q, k, v = cuda(x["q"]), cuda(x["k"]), cuda(x["v"])
+    scale = d ** -0.5
+    o, lse = run_fwd(q, k, v, causal, scale)
+    o_w = poisoned(q.shape, torch.bfloat16)
+    lse_w = poisoned(q.shape[:3], torch.float32)
+    fa.fa_fwd_window(q, k, v, o_w, lse_w, scale, -1, 0 if causal else -1)
+    fa.fa_sync_status()
+    assert torch.equal(o, o_w) and torch.equal(lse, lse_w)
+    for b, h in ((0, 0), (2, 17), (3, 31)):
+        o_ref, lse_ref = A.forward(x["q"][b:b + 1, h:h + 1], x["k"][b:b + 1, h:h + 1],
+                                   x["v"][b:b + 1, h:h + 1], scale, causal)
+        assert_o_close(o[b:b + 1, h:h + 1], o_ref)
+        assert_lse_close(lse[b:b + 1, h:h + 1], lse_ref)
