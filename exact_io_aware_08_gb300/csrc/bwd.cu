@@ -403,12 +403,24 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
     bool ok = true;
     for (int i = 0; i < n; ++i) {
       const int q0 = step_q0(i);
+      // -lse (log2 units) and -D of the step's columns, the same for every thread: lane l reads
+      // column l once and shuffles pass the values round (a uniform-address shared load costs a
+      // shared-memory wavefront per 4 bytes delivered).  The first 32 columns are fetched while
+      // the warps would otherwise wait for S_i: stage i is waited for directly here.
+      if (!(ok = mbar_wait_warp(&stage_full[i % C::NST], (i / C::NST) & 1, abort_flag, 225))) break;
+      const float* s_nlse = reinterpret_cast<const float*>(smem + C::OFF_LSE + (i % C::NST) * C::LSE_STAGE);
+      const float* s_nd = s_nlse + C::BM;
+      float lane_nd[C::HALF / 32], nl0[32];
+      {
+        const float lane_nl = s_nlse[cb + lane];
+        lane_nd[0] = s_nd[cb + lane];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) nl0[e] = __shfl_sync(0xffffffffu, lane_nl, e);
+      }
       // st_full(i): S_i is done, stage i (lse, D) is loaded and dS^T buffer i & 1 is free
       // (the last two folded in by the helper); dp_full(i), waited for below: dP_i is done
       if (!(ok = mbar_wait_warp(st_full, i & 1, abort_flag, 221))) break;
       tc_fence_after();
-      const float* s_nlse = reinterpret_cast<const float*>(smem + C::OFF_LSE + (i % C::NST) * C::LSE_STAGE);
-      const float* s_nd = s_nlse + C::BM;
       // a (key tile, query tile) pair that some pair of rows sees only in part
       const bool diag = WIN ? ((q0 < k0 + C::BN - 1 - wr) || (q0 + C::BM - 1 > k0 + wl))
                             : (p.causal && (q0 < k0 + C::BN - 1));
@@ -420,20 +432,22 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       // dV product reads it.  p_ready is signalled as soon as every thread has stored its P^T
       // and read its dP^T, so dV and the next S/dP products (which overwrite S^T and dP^T)
       // overlap the dS math below.
-      float pf[C::HALF], lane_nd[C::HALF / 32];
+      float pf[C::HALF];
       uint32_t dpu[C::HALF / 32][32];
 #pragma unroll
       for (int c = 0; c < C::HALF / 32; ++c) {
         uint32_t rs[32];
         tmem_ld32(tbase + t_lane + C::T_S + cb + c * 32, rs);
-        // per-column -lse (log2 units) and -D, the same for every thread: lane l reads column
-        // l once and shuffles pass the values round (a uniform-address shared load costs a
-        // shared-memory wavefront per 4 bytes delivered)
         float nl[32];
-        const float lane_nl = s_nlse[cb + c * 32 + lane];
-        lane_nd[c] = s_nd[cb + c * 32 + lane];
+        if (c == 0) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) nl[e] = __shfl_sync(0xffffffffu, lane_nl, e);
+          for (int e = 0; e < 32; ++e) nl[e] = nl0[e];
+        } else {
+          const float lane_nl = s_nlse[cb + c * 32 + lane];
+          lane_nd[c] = s_nd[cb + c * 32 + lane];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) nl[e] = __shfl_sync(0xffffffffu, lane_nl, e);
+        }
         tmem_wait_ld();
         uint32_t pk_p[16];
 #pragma unroll
