@@ -22,7 +22,7 @@ __all__ = [
     "fa_bwd_varlen", "backward_varlen", "fa_decode_paged", "decode_paged", "fa_fwd_fp8", "forward_fp8",
     "fa_fwd_window", "fa_bwd_window", "forward_window", "backward_window",
     "fa_fwd_block_sparse", "fa_bwd_block_sparse", "forward_block_sparse", "backward_block_sparse",
-    "BLOCK_SIZE",
+    "BLOCK_SIZE", "fa_debug_counters",
 ]
 
 BLOCK_SIZE = 128   # block-sparse attention: blocks of 128 queries x 128 keys
@@ -75,6 +75,7 @@ _SIGNATURES = {
                              _P]),
     "fa_sync_status": (_I, [_P]),
     "fa_selftest_wait_timeout": (_I, [ctypes.c_uint, _P]),
+    "fa_debug_counters": (_I, [_P]),
     "fa_status_string": (ctypes.c_char_p, [_I]),
     "fa_last_error_message": (ctypes.c_char_p, []),
 }
@@ -310,6 +311,12 @@ def fa_decode_paged(q, k_cache, v_cache, o, lse, block_table, seqlens_k, max_seq
                                           block_table.shape[1], block_size, num_blocks,
                                           int(max_seqlen_k), d, float(scale), int(n_splits),
                                           _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def fa_debug_counters(counters):
+    """Point the diagnostic tile counters at ``counters`` (a uint64/int64 device tensor of >= 2
+    entries), or turn them off with None (see include/fa.h)."""
+    _check(load_library().fa_debug_counters(None if counters is None else _ptr(counters)))
 
 
 def fa_sync_status(stream=None):

@@ -9,6 +9,12 @@
 #include "../../include/fa.h"
 #include "fa_kernels.h"
 
+namespace fa {
+// Process-wide diagnostic counters (fa_debug_counters); read by the launchers.
+unsigned long long* g_debug_counters = nullptr;
+unsigned long long* debug_counters() { return g_debug_counters; }
+}  // namespace fa
+
 namespace {
 
 thread_local char g_msg[512] = "no error";
@@ -494,6 +500,11 @@ fa_status_t fa_decode_paged(const fa_bf16_t* q, const fa_bf16_t* k_cache,
   a.chunk = fa::decode_chunk(max_seqlen_k, n_splits);
   cudaError_t e = fa::launch_decode_paged(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "fa_decode_paged launch");
+  return FA_OK;
+}
+
+fa_status_t fa_debug_counters(unsigned long long* device_counters) {
+  fa::g_debug_counters = device_counters;
   return FA_OK;
 }
 

@@ -104,6 +104,7 @@ struct BwdParams {
   // every head (bm_per_head = 0) or one such array per (b, h) plane.
   const uint8_t* block_mask;
   int bm_per_head, n_qblocks;
+  unsigned long long* stats;                        // diagnostic counters (see fa_kernels.h)
 };
 
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
@@ -389,6 +390,7 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       }
       umma_commit(mma_done);
       mbar_wait(mma_done, 0, nullptr, 217);
+      if (ok && p.stats != nullptr) atomicAdd(&p.stats[1], static_cast<unsigned long long>(n));
     }
   } else if (warp < 10) {
     // ------------------------------------------------------------------ dS warpgroups
@@ -746,6 +748,7 @@ static cudaError_t launch_bwd_main_d(const BwdArgs& a, cudaStream_t stream) {
   p.cu_q = p.cu_k = nullptr;
   p.dk = static_cast<uint16_t*>(a.dk);
   p.dv = static_cast<uint16_t*>(a.dv);
+  p.stats = debug_counters();
   attention_window(a.causal, a.windowed, a.win_left, a.win_right, &p.win_left, &p.win_right);
   p.block_mask = a.block_mask;
   p.bm_per_head = a.bm_per_head;
@@ -808,6 +811,7 @@ static cudaError_t launch_bwd_main_varlen_d(const BwdArgs& a, cudaStream_t strea
   p.cu_k = a.cu_k;
   p.dk = static_cast<uint16_t*>(a.dk);
   p.dv = static_cast<uint16_t*>(a.dv);
+  p.stats = debug_counters();
   attention_window(a.causal, false, 0, 0, &p.win_left, &p.win_right);
   p.block_mask = nullptr;
   p.bm_per_head = p.n_qblocks = 0;

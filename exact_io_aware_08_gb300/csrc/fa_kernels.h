@@ -20,6 +20,11 @@ enum DevError : unsigned int {
 // i - win_left <= j <= i + win_right.
 constexpr int kWinUnbounded = 1 << 30;
 
+// Diagnostic counters (device memory, set through fa_debug_counters; null = off): kernels add
+// [0] the forward S products (query tile x key tile) they computed, [1] the backward
+// (key tile, query step) pairs they visited.
+unsigned long long* debug_counters();
+
 // Block-sparse attention: blocks are 128 queries x 128 keys, and a call covers at most this
 // many key blocks (N_kv <= 131072), the length of the per-CTA stream list kept on chip.
 constexpr int kBlockSize = 128;

@@ -119,6 +119,7 @@ struct FwdParams {
   const uint8_t* block_mask;
   int bm_per_head, n_qblocks;
   int n_items;                                        // persistent forward: B*H*n_qpairs
+  unsigned long long* stats;                          // diagnostic counters (see fa_kernels.h)
 };
 
 template <int D, bool VL, bool F8 = false, bool WIN = false, bool BS = false>
@@ -323,7 +324,9 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 0, 1024);
       const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 0, 1024);
       const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), C::CHUNK, 1024);
+      unsigned long long n_s = 0;                               // S products issued
       auto issue_s = [&](int t, int j) {                        // S_t = Q_t K_j^T
+        ++n_s;
         const uint64_t a = desc_advance(dq0, t * C::TILE);
         const uint64_t b = desc_advance(dk0, (j % C::NS) * C::TILE);
         const uint32_t d_tmem = tbase + C::T_S + t * 128;
@@ -381,6 +384,7 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
           if (j + 1 < n_max) umma_commit(&k_empty[(j + 1) % C::NS]);
         }
       }
+      if (leader && p.stats != nullptr) atomicAdd(&p.stats[0], n_s);
     }
   } else if (C::NAMED_P && warp == 2) {
     // ------------------------------------------------------------------ helper (fp8)
@@ -418,7 +422,9 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 0, 1024);
       const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 0, 1024);
       const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), C::CHUNK, 1024);
+      unsigned long long n_s = 0;                               // S products issued
       auto issue_s = [&](int t, int j) {                        // S_t = Q_t K_j^T
+        ++n_s;
         const uint64_t a = desc_advance(dq0, t * C::TILE);
         const uint64_t b = desc_advance(dk0, (j % C::NS) * C::TILE);
         const uint32_t d_tmem = tbase + C::T_S + t * 128;
@@ -509,6 +515,7 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
         umma_commit(&v_empty[s]);
         if (j + 1 < n_max) umma_commit(&k_empty[(j + 1) % C::NS]);
       }
+      if (p.stats != nullptr) atomicAdd(&p.stats[0], n_s);
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------------ helper
@@ -930,7 +937,9 @@ fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
       const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 0, 1024);
       const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 0, 1024);
       const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), C::CHUNK, 1024);
+      unsigned long long n_s = 0;                              // S products issued
       auto issue_s = [&](int t, uint32_t P) {                  // S_t = Q_t K^T (position P)
+        ++n_s;
         const uint64_t a = desc_advance(dq0, t * C::TILE);
         const uint64_t b = desc_advance(dk0, (P % C::NS) * C::TILE);
 #pragma unroll
@@ -984,6 +993,7 @@ fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
         for (int t = 0; t < 2; ++t) act[t] += it.n_t[t] > 0;
         P += it.n_max;
       }
+      if (p.stats != nullptr) atomicAdd(&p.stats[0], n_s);
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------------ helper
@@ -1199,6 +1209,7 @@ static cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   p.cu_q = p.cu_k = nullptr;
   p.o = static_cast<uint16_t*>(a.o);
   p.out_scale = 1.f;
+  p.stats = debug_counters();
   attention_window(a.causal, a.windowed, a.win_left, a.win_right, &p.win_left, &p.win_right);
   p.block_mask = a.block_mask;
   p.bm_per_head = a.bm_per_head;
@@ -1268,6 +1279,7 @@ static cudaError_t launch_fwd_varlen_d(const FwdVarlenArgs& a, cudaStream_t stre
   p.cu_k = a.cu_k;
   p.o = static_cast<uint16_t*>(a.o);
   p.out_scale = 1.f;
+  p.stats = debug_counters();
   attention_window(a.causal, false, 0, 0, &p.win_left, &p.win_right);
   p.block_mask = nullptr;
   p.bm_per_head = p.n_qblocks = 0;
@@ -1306,6 +1318,7 @@ cudaError_t launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream) {
   p.cu_q = p.cu_k = nullptr;
   p.o = static_cast<uint16_t*>(a.o);
   p.out_scale = a.descale_v;
+  p.stats = debug_counters();
   attention_window(a.causal, false, 0, 0, &p.win_left, &p.win_right);
   p.block_mask = nullptr;
   p.bm_per_head = p.n_qblocks = 0;

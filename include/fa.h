@@ -320,6 +320,21 @@ fa_status_t fa_sync_status(void* stream);
  */
 fa_status_t fa_selftest_wait_timeout(unsigned int limit_us, void* stream);
 
+/*
+ * fa_debug_counters -- diagnostic counters of the tile skipping ([Lesson4] "Causal masks": the
+ * kernel skips tiles above the diagonal and computes T(T+1)/2 of the T^2 tiles; the same
+ * skipping serves sliding windows and block masks).
+ *
+ * device_counters: a DEVICE array of at least 2 unsigned 64-bit counters owned by the caller,
+ * or NULL to turn counting off (the default).  While set (process-wide, for launches issued
+ * after the call), every forward kernel adds to [0] the number of S = Q K^T tile products
+ * (128-query tile x 128-key tile) it computed, and every backward main kernel adds to [1] the
+ * number of (128-key tile, query step) pairs it visited (a query step is 64 queries at d = 128,
+ * 128 at d = 64).  The caller zeroes the counters and reads them after synchronising.
+ * Always FA_OK.
+ */
+fa_status_t fa_debug_counters(unsigned long long* device_counters);
+
 /* Static, human-readable name of a status code. */
 const char* fa_status_string(fa_status_t status);
 
