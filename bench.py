@@ -282,14 +282,26 @@ def run_ours(args, rank, world, local_rank):
             main_events[1].record(stream)
         fa.fa_bwd_finish(d["dq"], d["ws"], w.N_kv, w.scale)
 
-    def timed(fn, steps, inner=False):
-        """Warm up, then time ``steps`` calls between barriers; optional per-call events."""
+    def nvtx(push, label=None):
+        """NVTX range markers; a no-op where this torch build has none."""
+        try:
+            if push:
+                torch.cuda.nvtx.range_push(label)
+            else:
+                torch.cuda.nvtx.range_pop()
+        except (AttributeError, RuntimeError):
+            pass
+
+    def timed(fn, steps, inner=False, name=None):
+        """Warm up, then time ``steps`` calls between barriers; optional per-call events.  The
+        timed region is an NVTX range (named after the timed function) for profiler timelines."""
         for _ in range(Wm):
             fn(None)
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
         s, e = ev(), ev()
+        nvtx(True, name or getattr(fn, "__name__", "timed"))
         s.record(stream)
         per = []
         for _ in range(steps):
@@ -298,6 +310,7 @@ def run_ours(args, rank, world, local_rank):
             if inner:
                 per.append(pe)
         e.record(stream)
+        nvtx(False)
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()

@@ -2,6 +2,7 @@
 // to the kernel launchers, device-status collection.  Nothing here allocates memory or falls
 // back to another implementation: an unsupported call returns an error before any launch.
 #include <cmath>
+#include <cstdlib>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -13,6 +14,14 @@ namespace fa {
 // Process-wide diagnostic counters (fa_debug_counters); read by the launchers.
 unsigned long long* g_debug_counters = nullptr;
 unsigned long long* debug_counters() { return g_debug_counters; }
+
+void log_launch(const char* kernel, unsigned long long grid, unsigned threads, unsigned long long smem) {
+  static const bool on = [] {
+    const char* v = std::getenv("FA_LOG");
+    return v != nullptr && v[0] != '\0' && std::strcmp(v, "0") != 0;
+  }();
+  if (on) std::fprintf(stderr, "[fa] launch %s grid=%llu block=%u smem=%llu\n", kernel, grid, threads, smem);
+}
 }  // namespace fa
 
 namespace {

@@ -710,6 +710,7 @@ static cudaError_t launch_bwd_prep_d(const BwdArgs& a, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
   const long long acc4 = rows * D / 4;
   const int blocks = static_cast<int>(std::min<long long>(152LL * 8, (rows * (D / 8) + 255) / 256));
+  log_launch("bwd_pre_kernel<D>", static_cast<unsigned long long>(std::max(blocks, 1)), 256, static_cast<unsigned long long>(0));
   bwd_pre_kernel<D><<<std::max(blocks, 1), 256, 0, stream>>>(
       static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dO), a.delta,
       reinterpret_cast<float4*>(a.dq_acc), rows, acc4);
@@ -759,6 +760,7 @@ static cudaError_t launch_bwd_main_d(const BwdArgs& a, cudaStream_t stream) {
     static int attr_bs[64] = {0};
     cudaError_t e = ensure_smem_attr(bwd_main_kernel<D, false, false, true>, C::SMEM_BYTES, attr_bs);
     if (e != cudaSuccess) return e;
+    log_launch("bwd_main_kernel<D, false, false, true>", static_cast<unsigned long long>(static_cast<unsigned>(grid)), C::THREADS, static_cast<unsigned long long>(C::SMEM_BYTES));
     bwd_main_kernel<D, false, false, true><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
   }
@@ -766,11 +768,13 @@ static cudaError_t launch_bwd_main_d(const BwdArgs& a, cudaStream_t stream) {
     static int attr_win[64] = {0};
     cudaError_t e = ensure_smem_attr(bwd_main_kernel<D, false, true>, C::SMEM_BYTES, attr_win);
     if (e != cudaSuccess) return e;
+    log_launch("bwd_main_kernel<D, false, true>", static_cast<unsigned long long>(static_cast<unsigned>(grid)), C::THREADS, static_cast<unsigned long long>(C::SMEM_BYTES));
     bwd_main_kernel<D, false, true><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
   }
   cudaError_t e = ensure_smem_attr(bwd_main_kernel<D, false>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
+  log_launch("bwd_main_kernel<D, false>", static_cast<unsigned long long>(static_cast<unsigned>(grid)), C::THREADS, static_cast<unsigned long long>(C::SMEM_BYTES));
   bwd_main_kernel<D, false><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
@@ -819,6 +823,7 @@ static cudaError_t launch_bwd_main_varlen_d(const BwdArgs& a, cudaStream_t strea
   cudaError_t e = ensure_smem_attr(bwd_main_kernel<D, true>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
   const uint64_t grid = static_cast<uint64_t>(p.n_kvtiles) * a.n_seqs * a.H;
+  log_launch("bwd_main_kernel<D, true>", static_cast<unsigned long long>(static_cast<unsigned>(grid)), C::THREADS, static_cast<unsigned long long>(C::SMEM_BYTES));
   bwd_main_kernel<D, true><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
@@ -829,6 +834,7 @@ static cudaError_t launch_bwd_finish_d(const BwdArgs& a, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
   const long long n4 = rows * D / 4;
   const int blocks = static_cast<int>(std::min<long long>(152LL * 8, (n4 + 255) / 256));
+  log_launch("bwd_dq_convert_kernel", static_cast<unsigned long long>(std::max(blocks, 1)), 256, static_cast<unsigned long long>(0));
   bwd_dq_convert_kernel<<<std::max(blocks, 1), 256, 0, stream>>>(
       reinterpret_cast<const float4*>(a.dq_acc), static_cast<uint2*>(a.dq), a.scale, n4);
   return cudaGetLastError();

@@ -343,9 +343,11 @@ static cudaError_t launch_decode_d(const DecodeArgs& a, cudaStream_t stream) {
   cudaError_t e = ensure_smem_attr(decode_split_kernel<D, false>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
   const int grid = min(p.n_items, 2 * sm_count());
+  log_launch("decode_split_kernel<D, false>", static_cast<unsigned long long>(grid), C::THREADS, static_cast<unsigned long long>(C::SMEM_BYTES));
   decode_split_kernel<D, false><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  log_launch("decode_merge_kernel<D>", static_cast<unsigned long long>(static_cast<unsigned>(bh)), D, static_cast<unsigned long long>(0));
   decode_merge_kernel<D><<<static_cast<unsigned>(bh), D, 0, stream>>>(
       a.part, static_cast<uint16_t*>(a.o), a.lse, a.n_splits);
   return cudaGetLastError();
@@ -379,9 +381,11 @@ static cudaError_t launch_decode_paged_d(const DecodePagedArgs& a, cudaStream_t 
   cudaError_t e = ensure_smem_attr(decode_split_kernel<D, true>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
   const int grid = min(p.n_items, 2 * sm_count());
+  log_launch("decode_split_kernel<D, true>", static_cast<unsigned long long>(grid), C::THREADS, static_cast<unsigned long long>(C::SMEM_BYTES));
   decode_split_kernel<D, true><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  log_launch("decode_merge_kernel<D>", static_cast<unsigned long long>(static_cast<unsigned>(bh)), D, static_cast<unsigned long long>(0));
   decode_merge_kernel<D><<<static_cast<unsigned>(bh), D, 0, stream>>>(
       a.part, static_cast<uint16_t*>(a.o), a.lse, a.n_splits);
   return cudaGetLastError();

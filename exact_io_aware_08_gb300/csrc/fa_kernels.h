@@ -25,6 +25,10 @@ constexpr int kWinUnbounded = 1 << 30;
 // (key tile, query step) pairs they visited.
 unsigned long long* debug_counters();
 
+// Host-side launch log: with the environment variable FA_LOG set to a non-empty value other
+// than 0, every kernel launch is written to stderr (kernel, grid, block, dynamic shared memory).
+void log_launch(const char* kernel, unsigned long long grid, unsigned threads, unsigned long long smem);
+
 // Block-sparse attention: blocks are 128 queries x 128 keys, and a call covers at most this
 // many key blocks (N_kv <= 131072), the length of the per-CTA stream list kept on chip.
 constexpr int kBlockSize = 128;

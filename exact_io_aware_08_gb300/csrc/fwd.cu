@@ -1220,6 +1220,7 @@ static cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
     static int attr_bs[64] = {0};
     cudaError_t e = ensure_smem_attr(fwd_kernel<D, false, false, false, true>, C::SMEM_BYTES, attr_bs);
     if (e != cudaSuccess) return e;
+    log_launch("fwd_kernel<D, false, false, false, true>", static_cast<unsigned long long>(static_cast<unsigned>(grid)), C::THREADS, static_cast<unsigned long long>(C::SMEM_BYTES));
     fwd_kernel<D, false, false, false, true><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
   }
@@ -1236,6 +1237,7 @@ static cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     p.n_items = static_cast<int>(grid);
     const unsigned ctas = static_cast<unsigned>(std::min<uint64_t>(grid, static_cast<uint64_t>(std::max(sms, 1))));
+    log_launch("fwd_persistent_kernel<D>", static_cast<unsigned long long>(ctas), PC::THREADS, static_cast<unsigned long long>(PC::SMEM_BYTES));
     fwd_persistent_kernel<D><<<ctas, PC::THREADS, PC::SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
   }
@@ -1243,11 +1245,13 @@ static cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
     static int attr_win[64] = {0};
     cudaError_t e = ensure_smem_attr(fwd_kernel<D, false, false, true>, C::SMEM_BYTES, attr_win);
     if (e != cudaSuccess) return e;
+    log_launch("fwd_kernel<D, false, false, true>", static_cast<unsigned long long>(static_cast<unsigned>(grid)), C::THREADS, static_cast<unsigned long long>(C::SMEM_BYTES));
     fwd_kernel<D, false, false, true><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
   }
   cudaError_t e = ensure_smem_attr(fwd_kernel<D, false>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
+  log_launch("fwd_kernel<D, false>", static_cast<unsigned long long>(static_cast<unsigned>(grid)), C::THREADS, static_cast<unsigned long long>(C::SMEM_BYTES));
   fwd_kernel<D, false><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
@@ -1288,6 +1292,7 @@ static cudaError_t launch_fwd_varlen_d(const FwdVarlenArgs& a, cudaStream_t stre
   if (e != cudaSuccess) return e;
   const uint64_t grid = static_cast<uint64_t>(p.n_qpairs) * a.n_seqs * a.H;
   if (grid == 0) return cudaSuccess;
+  log_launch("fwd_kernel<D, true>", static_cast<unsigned long long>(static_cast<unsigned>(grid)), C::THREADS, static_cast<unsigned long long>(C::SMEM_BYTES));
   fwd_kernel<D, true><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }
@@ -1326,6 +1331,7 @@ cudaError_t launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream) {
   cudaError_t e = ensure_smem_attr(fwd_kernel<D, false, true>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;
   const uint64_t grid = static_cast<uint64_t>(p.n_qpairs) * bh;
+  log_launch("fwd_kernel<D, false, true>", static_cast<unsigned long long>(static_cast<unsigned>(grid)), C::THREADS, static_cast<unsigned long long>(C::SMEM_BYTES));
   fwd_kernel<D, false, true><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
   return cudaGetLastError();
 }

@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(32, 1) selftest_wait_kernel(unsigned long long
 }
 
 cudaError_t launch_selftest_wait(unsigned long long limit_ns, cudaStream_t stream) {
+  log_launch("selftest_wait_kernel", static_cast<unsigned long long>(1), 32, static_cast<unsigned long long>(0));
   selftest_wait_kernel<<<1, 32, 0, stream>>>(limit_ns);
   return cudaGetLastError();
 }

@@ -39,3 +39,24 @@ def test_timeout_on_a_side_stream_is_seen_by_sync_status_of_that_stream():
         fa.fa_sync_status(stream=s)
     assert e.value.status == TIMEOUT
     fa.fa_sync_status(stream=s)
+
+
+def test_fa_log_writes_one_line_per_launch():
+    """FA_LOG=1 makes every launch print its kernel and launch shape to stderr (host side)."""
+    import os
+    import subprocess
+    import sys
+    require_gpu()
+    code = ("import torch, exact_io_aware_08_gb300 as fa\n"
+            "q = torch.randn(1, 2, 300, 64, device='cuda').to(torch.bfloat16)\n"
+            "o, lse = fa.forward(q, q, q, causal=True)\n"
+            "torch.cuda.synchronize()\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                       env={**os.environ, "FA_LOG": "1"}, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stderr.splitlines() if l.startswith("[fa] launch ")]
+    assert len(lines) == 1 and "grid=" in lines[0] and "smem=" in lines[0], r.stderr[-2000:]
+    r0 = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                        env={k: v for k, v in os.environ.items() if k != "FA_LOG"}, timeout=300)
+    assert r0.returncode == 0 and "[fa] launch" not in r0.stderr
