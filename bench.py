@@ -18,6 +18,8 @@ Also measured in the same run and reported in the same JSON line:
                            on 1x16x16384x128
   breakdown.block_sparse   the same shape under a causal 128x128 block pattern (a band of one
                            block, the first key block, 5% random blocks)
+  breakdown.varlen         a packed batch of 16 causal sequences of 512..8192 tokens (H=32,
+                           d=128), forward and forward+backward
   roofline                 the dominant kernel of the step (backward main kernel), timed alone
   e2e                      the step through the public Python API with host (pinned) buffers,
                            host->device and device->host copies inside the timed region
@@ -478,6 +480,41 @@ def run_ours(args, rank, world, local_rank):
         "flops": "4 d (fwd) and 10 d (bwd) per visible (query, key) pair",
     }
     del xw, ow, lw, gw, wsw, bmask_d
+
+    # ---- variable-length batch: 16 packed causal sequences of 512..8192 tokens, 32 heads, d=128
+    vlens = inputs.make_varlen_lengths(16, 512, 8192, 1006)
+    vH, vd = 32, 128
+    vtot = sum(vlens)
+    xv = inputs.make_packed(vtot, vH, vd, 1006 + 7919 * rank, device=str(dev))
+    vcu = torch.tensor([sum(vlens[:i]) for i in range(len(vlens) + 1)], dtype=torch.int32, device=dev)
+    vmax = max(vlens)
+    ov = torch.empty_like(xv["q"])
+    lv = torch.empty((vH, vtot), dtype=torch.float32, device=dev)
+    gv = [torch.empty_like(xv["q"]) for _ in range(3)]
+    wsv = torch.empty(fa.fa_bwd_workspace_size(1, vH, vtot, vtot, vd), dtype=torch.uint8, device=dev)
+    vpairs = sum(W.pairs(n_, n_, True) for n_ in vlens) * vH
+    fl_vf, fl_vb = 4 * vd * vpairs, 10 * vd * vpairs
+    vscale = vd ** -0.5
+
+    def vl_fwd(pe):
+        fa.fa_fwd_varlen(xv["q"], xv["k"], xv["v"], ov, lv, vcu, vcu, vmax, vmax, vscale, True)
+
+    def vl_step(pe):
+        vl_fwd(pe)
+        fa.fa_bwd_varlen(xv["q"], xv["k"], xv["v"], ov, lv, xv["do"], gv[0], gv[1], gv[2], wsv, vcu, vcu,
+                         vmax, vmax, vscale, True)
+    vf_total, _ = timed(vl_fwd, K)
+    vb_total, _ = timed(vl_step, K)
+    vf_ms, vb_ms = reduce_max(vf_total / K), reduce_max(vb_total / K)
+    breakdown["varlen"] = {
+        "workload": f"16 packed causal sequences of 512..8192 tokens (seed 1006: {vtot} tokens in all), "
+                    f"H={vH}, d={vd}",
+        "fwd_tflops": round(whole_job_rate(fl_vf, world, vf_ms * 1e-3) / 1e12, 1), "fwd_ms": round(vf_ms, 4),
+        "fwd_bwd_tflops": round(whole_job_rate(fl_vf + fl_vb, world, vb_ms * 1e-3) / 1e12, 1),
+        "fwd_bwd_ms": round(vb_ms, 4),
+        "flops": "4 d (fwd) and 10 d (bwd) per visible (query, key) pair of each sequence",
+    }
+    del xv, ov, lv, gv, wsv
 
     # ---- FP8 forward (e4m3 Q, K, V with per-tensor scales) on the same shapes
     x8 = inputs.make_qkv_fp8(w.B, w.H, w.N_q, w.N_kv, w.d, w.seed + 7919 * rank, device=str(dev))

@@ -129,3 +129,18 @@ def make_block_mask(n_qblocks: int, n_kblocks: int, seed: int, *, band: int = 1,
     m |= (j - i).abs() <= band
     m |= j < n_global
     return m.to(torch.uint8)
+
+
+def make_varlen_lengths(n_seqs: int, lo: int, hi: int, seed: int) -> list[int]:
+    """Seeded sequence lengths, uniform in [lo, hi], for a packed variable-length batch."""
+    gen = torch.Generator().manual_seed(seed)
+    return [int(x) for x in torch.randint(lo, hi + 1, (n_seqs,), generator=gen)]
+
+
+def make_packed(total: int, H: int, d: int, seed: int, *, device: str, with_do: bool = True):
+    """Packed token-major [total, H, d] Q, K, V (and dO): fp32 N(0,1) draws from a seeded CUDA
+    generator rounded to bf16 (the recipe of ``make_qkv``, drawn on the device because benchmark
+    batches are large)."""
+    gen = torch.Generator(device=device).manual_seed(seed)
+    names = ("q", "k", "v", "do") if with_do else ("q", "k", "v")
+    return {n: torch.randn((total, H, d), generator=gen, device=device).to(torch.bfloat16) for n in names}
