@@ -31,6 +31,10 @@
 //       the dQ drain of step i overlaps the dQ product of step i+1.
 //       d = 128 uses 64-query steps and forms dQ^T = K^T dS^T (d on TMEM lanes);
 //       d = 64 uses 128-query steps and forms dQ = dS K (queries on TMEM lanes).
+//       S^T and dP^T are committed separately, so the dS warps exponentiate while dP^T runs.
+//       Variants (template flags): VL -- packed variable-length batches; WIN -- a sliding
+//       window (only the query tiles some row of the key tile sees); BS -- a block mask (only
+//       the query blocks set with the key tile, found from a bit array of the mask column).
 //   F4  bwd_dq_convert: dq = bf16(scale * dQ_acc).
 #include <algorithm>
 

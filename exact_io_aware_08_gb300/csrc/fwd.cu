@@ -30,7 +30,10 @@
 // Variants (template flags): VL -- packed variable-length batches (one work item per sequence,
 // head and 256-row block); F8 -- e4m3 Q, K, V (tcgen05.mma kind::f8f6f4, K = 32 per
 // instruction, P stored as e4m3 four per TMEM column over the first 32 columns of S_t); WIN --
-// a sliding window (each query tile streams only the key tiles its rows can see).
+// a sliding window (each query tile streams only the key tiles its rows can see); BS -- a block
+// mask (the CTA streams the union of its two query tiles' set key blocks, each tile computes
+// only its own).  Heads of at most kPersistentMaxKvTiles key tiles run on
+// fwd_persistent_kernel (below), which walks several work items per CTA.
 //
 // Rescaling.  The online-softmax theorem holds for ANY reference value that l and o~ share:
 // o~/l is unchanged when both are measured against a stale maximum.  So a row moves its
