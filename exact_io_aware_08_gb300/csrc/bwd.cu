@@ -623,7 +623,9 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
           bulk_commit_group();
         }
       }
-      if (leader) bulk_wait_group0();
+      // the staging box must stay readable until the last reduce has read it; its adds into
+      // the accumulator complete on their own (as a TMA store's writes do)
+      if (leader) bulk_wait_group_read0();
     } else {
       for (int i = 0; i < n; ++i) {
         const int q0 = step_q0(i);
