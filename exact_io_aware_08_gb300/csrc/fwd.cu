@@ -775,8 +775,8 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
 
 // ------------------------------------------------------------------------------------------
 // Persistent forward (plain bf16: no window, block mask, varlen or fp8).  One CTA per SM walks
-// the work items blockIdx.x, blockIdx.x + gridDim.x, ... (the same items, in the same
-// longest-first order, as one CTA per item), so that one item's tail overlaps the next one's
+// the work items (the same items as one CTA per item, taken longest first in rounds of
+// gridDim.x, zig-zag: pers_item), so that one item's tail overlaps the next one's
 // start: the next item's Q is loaded as soon as the current item's last S products complete,
 // its first S products follow the last PV products, and the softmax warps store the finished
 // item's O (through a staging buffer the two tiles take in turn) while the tensor core works.
@@ -818,10 +818,18 @@ struct FwdItem {
   int bh, q0[2], n_t[2], n_max;
 };
 
+// Item k of this CTA: rounds of gridDim.x items, walked forward in even rounds and backward in
+// odd ones, so that with items ordered longest first every CTA gets a similar total.
+__device__ __forceinline__ int pers_item(int k, int G) {
+  return k * G + ((k & 1) ? G - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
+}
+
 __device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int item) {
   FwdItem it;
-  int bh = item / p.n_qpairs, r = item % p.n_qpairs;
-  if (p.causal) causal_item(item, p.n_items / p.n_qpairs, p.n_qpairs, &bh, &r);
+  // rank-major: every head's longest item (causal), then every head's second, ...; the short
+  // heads this kernel serves keep all their K/V in L2 at once
+  const int n_bh = p.n_items / p.n_qpairs;
+  const int bh = item % n_bh, r = item / n_bh;
   const int c = p.causal ? (p.n_qpairs - 1 - r) : r;
   it.bh = bh;
 #pragma unroll
@@ -899,8 +907,8 @@ fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
       uint32_t P = 0, issued = 0;             // stream positions over all items
       int nq = 0;                             // Q loads issued
       bool ok = true;
-      for (int k = 0; ok && blockIdx.x + k * G < p.n_items; ++k) {
-        const FwdItem it = fwd_item(p, blockIdx.x + k * G);
+      for (int k = 0; ok && pers_item(k, G) < p.n_items; ++k) {
+        const FwdItem it = fwd_item(p, pers_item(k, G));
         if (k > 0 && !(ok = mbar_wait(q_empty, (k - 1) & 1, abort_flag, 141))) break;
         mbar_arrive_expect_tx(q_full, ((it.n_t[0] > 0) + (it.n_t[1] > 0)) * C::TILE);
         for (int t = 0; t < 2; ++t)
@@ -961,8 +969,8 @@ fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
       };
       uint32_t P = 0, cp[2] = {0, 0}, act[2] = {0, 0};
       bool ok = true;
-      for (int k = 0; ok && blockIdx.x + k * G < p.n_items; ++k) {
-        const FwdItem it = fwd_item(p, blockIdx.x + k * G);
+      for (int k = 0; ok && pers_item(k, G) < p.n_items; ++k) {
+        const FwdItem it = fwd_item(p, pers_item(k, G));
         if (!(ok = mbar_wait(q_full, k & 1, abort_flag, 151) &&
                    mbar_wait(&k_full[P % C::NS], (P / C::NS) & 1, abort_flag, 152)))
           break;
@@ -1005,8 +1013,8 @@ fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
     if (lane == 0) {
       uint32_t P = 0, ch[2] = {0, 0};
       bool ok = true;
-      for (int k = 0; ok && blockIdx.x + k * G < p.n_items; ++k) {
-        const FwdItem it = fwd_item(p, blockIdx.x + k * G);
+      for (int k = 0; ok && pers_item(k, G) < p.n_items; ++k) {
+        const FwdItem it = fwd_item(p, pers_item(k, G));
         for (int j = 0; ok && j < it.n_max; ++j) {
           const uint32_t Pj = P + j;
           if (!(ok = mbar_wait(&v_full[Pj % C::NS], (Pj / C::NS) & 1, abort_flag, 161))) break;
@@ -1039,8 +1047,8 @@ fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
     const float2 c2v = make_float2(c2, c2);
     uint32_t cs = 0, act = 0, uses = 0;       // S hand-offs, items of this tile, staging uses
     bool ok = true;
-    for (int k = 0; ok && blockIdx.x + k * G < p.n_items; ++k) {
-      const FwdItem it = fwd_item(p, blockIdx.x + k * G);
+    for (int k = 0; ok && pers_item(k, G) < p.n_items; ++k) {
+      const FwdItem it = fwd_item(p, pers_item(k, G));
       // the staging buffer goes to the items' active tiles in order: tile 0, then tile 1
       const uint32_t my_use = uses + ((t == 1 && it.n_t[0] > 0) ? 1u : 0u);
       uses += (it.n_t[0] > 0) + (it.n_t[1] > 0);
