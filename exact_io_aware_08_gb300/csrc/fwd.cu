@@ -32,8 +32,8 @@
 // instruction, P stored as e4m3 four per TMEM column over the first 32 columns of S_t); WIN --
 // a sliding window (each query tile streams only the key tiles its rows can see); BS -- a block
 // mask (the CTA streams the union of its two query tiles' set key blocks, each tile computes
-// only its own).  Heads of at most kPersistentMaxKvTiles key tiles run on
-// fwd_persistent_kernel (below), which walks several work items per CTA.
+// only its own).  Short heads (use_persistent) run on fwd_persistent_kernel (below), which
+// walks several work items per CTA.
 //
 // Rescaling.  The online-softmax theorem holds for ANY reference value that l and o~ share:
 // o~/l is unchanged when both are measured against a stale maximum.  So a row moves its
@@ -783,8 +783,13 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
 // Every mbarrier phase is counted across items.  Roles, TMEM and the online softmax are those
 // of fwd_kernel.
 // ------------------------------------------------------------------------------------------
-// Heads of at most this many key tiles run on the persistent forward.
-constexpr int kPersistentMaxKvTiles = 8;
+// Heads short enough for the persistent forward: it pays when a work item is a few tiles long
+// (measured on GB300: up to 16 key tiles for causal heads, whose items average half the head,
+// and for d = 64; up to 8 for unmasked d = 128, where at 16 it was 3% slower).
+constexpr int kPersistentMaxKvTiles = 16;
+__host__ __device__ constexpr bool use_persistent(int d, bool causal, int n_kvtiles) {
+  return n_kvtiles <= ((causal || d == 64) ? kPersistentMaxKvTiles : kPersistentMaxKvTiles / 2);
+}
 
 template <int D>
 struct FwdPCfg {
@@ -1235,7 +1240,7 @@ static cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
     fwd_kernel<D, false, false, false, true><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
   }
-  if (!a.windowed && a.n_kv > 0 && p.n_kvtiles <= kPersistentMaxKvTiles) {
+  if (!a.windowed && a.n_kv > 0 && use_persistent(D, a.causal != 0, p.n_kvtiles)) {
     // short items: the persistent kernel, one CTA per SM over the same items (measured: the
     // overlap at item boundaries pays when an item streams few key tiles; with long items the
     // one-CTA-per-item kernel runs its steps faster and wins)
