@@ -22,9 +22,10 @@
 //                    (bf16) goes to shared memory, where the dK and dQ products read it.
 //                    Epilogue: one group writes dV, the other dK (times scale), via TMA.
 //         warps 10-13 drain the dQ tile from TMEM into the fp32 accumulator, overlapping the
-//                    next tile's MMAs: d = 128 through a row-major fp32 box in shared memory
-//                    and one TMA reduce-add per step, d = 64 with vector reductions
-//                    (red.global.add).
+//                    next tile's MMAs, through an fp32 box in shared memory and TMA
+//                    reduce-adds (the L2 performs the adds): d = 128 a row-major box of its
+//                    own, d = 64 the step's dS^T buffer (dead once the step's dK and dQ
+//                    products are done), in the 128-byte-swizzled layout.
 //         warp 14    helper: folds the waits that do not depend on the dS math (stage loaded,
 //                    dS^T and dQ buffers free) into the hand-offs the MMA thread waits on.
 //       TMEM (512 columns): dV, dK (d each), S^T, dP^T (BM each), two dQ tiles (64 each), so
@@ -35,6 +36,8 @@
 //       Variants (template flags): VL -- packed variable-length batches; WIN -- a sliding
 //       window (only the query tiles some row of the key tile sees); BS -- a block mask (only
 //       the query blocks set with the key tile, found from a bit array of the mask column).
+//       Short heads at d = 64 run on bwd_persistent_kernel64 (below): the same roles and
+//       products, one CTA per SM walking (head, key tile) items.
 //   F4  bwd_dq_convert: dq = bf16(scale * dQ_acc).
 #include <algorithm>
 
@@ -68,8 +71,8 @@ struct BwdCfg {
   static constexpr int LSE_STAGE = 2 * BM * 4;
   static constexpr int OFF_BAR = OFF_LSE + NST * LSE_STAGE;
   // kv_full, stage_full[NST], stage_empty[NST], st_full, dp_full, p_ready, ds_ready,
-  // pds_free[2], dq_full[2], dq_free[2], mma_done, dqs_sync
-  static constexpr int NBAR = 1 + 2 * NST + 12;
+  // pds_free[2], dq_full[2], dq_free[2], mma_done, dqs_sync, dqs_done[2]
+  static constexpr int NBAR = 1 + 2 * NST + 14;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;       // TMEM slot, abort flag, step count
   // block-sparse: one bit per query block, set where this CTA's key tile has work
   static constexpr int OFF_BSW = OFF_MISC + 16;
@@ -89,7 +92,7 @@ struct BwdCfg {
 
 struct BwdParams {
   CUtensorMap tq, tk, tv, tdo, tdk, tdv;
-  CUtensorMap tdq;                                  // fp32 dQ accumulator (d = 128)
+  CUtensorMap tdq;                                  // fp32 dQ accumulator
   const float* lse;
   const float* delta;
   float* dq_acc;
@@ -109,16 +112,8 @@ struct BwdParams {
   const uint8_t* block_mask;
   int bm_per_head, n_qblocks;
   unsigned long long* stats;                        // diagnostic counters (see fa_kernels.h)
+  int n_items;                                      // persistent backward: B*H*n_kvtiles
 };
-
-__device__ __forceinline__ void red_add_f32(float* p, float v) {
-  asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" :: "l"(p), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ void red_add_v4_f32(float* p, float a, float b, float c, float d) {
-  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
-               :: "l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
-}
 
 template <int D, bool VL, bool WIN = false, bool BS = false>
 __global__ void __launch_bounds__(BwdCfg<D>::THREADS, 1)
@@ -142,6 +137,7 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
   uint64_t* dq_free = dq_full + 2;       // [2]
   uint64_t* mma_done = dq_free + 2;
   uint64_t* dqs_sync = mma_done + 1;     // the four dQ warps around the staging buffer
+  uint64_t* dqs_done = dqs_sync + 1;     // [2] d = 64: dQ staged in dS^T buffer b read by the TMA
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
 
@@ -253,6 +249,8 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
     }
     mbar_init(mma_done, 1);
     mbar_init(dqs_sync, 4);
+    mbar_init(&dqs_done[0], 1);
+    mbar_init(&dqs_done[1], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -438,7 +436,13 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       // dV product reads it.  p_ready is signalled as soon as every thread has stored its P^T
       // and read its dP^T, so dV and the next S/dP products (which overwrite S^T and dP^T)
       // overlap the dS math below.
-      float pf[C::HALF];
+      // d = 64 (64 columns a thread) keeps P for the dS product as the bf16 pairs it stores for
+      // the dV product: fp32 P would not fit the 128 registers a thread has with 15 warps (the
+      // spills cost more than the rounding, which stays below dS's own bf16 rounding); d = 128
+      // keeps fp32 P
+      constexpr bool kPackedP = (D == 64);
+      float pf[kPackedP ? 1 : C::HALF];
+      uint32_t ppk[kPackedP ? C::HALF / 2 : 1];
       uint32_t dpu[C::HALF / 32][32];
 #pragma unroll
       for (int c = 0; c < C::HALF / 32; ++c) {
@@ -470,9 +474,13 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
             if (row_dead || (diag && k_idx > q0 + col)) p0 = 0.f;
             if (row_dead || (diag && k_idx > q0 + col + 1)) p1 = 0.f;
           }
-          pf[c * 32 + e] = p0;
-          pf[c * 32 + e + 1] = p1;
           pk_p[e / 2] = pack_bf16x2(p0, p1);
+          if constexpr (kPackedP) {
+            ppk[c * 16 + e / 2] = pk_p[e / 2];
+          } else {
+            pf[c * 32 + e] = p0;
+            pf[c * 32 + e + 1] = p1;
+          }
         }
         tmem_st16(tbase + t_lane + C::T_S + cb + c * 16, pk_p);
       }
@@ -490,7 +498,12 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
         const float2 dp = make_float2(__uint_as_float(dpu[e / 32][e % 32]), __uint_as_float(dpu[e / 32][e % 32 + 1]));
         const float2 nd = make_float2(__shfl_sync(0xffffffffu, lane_nd[e / 32], e % 32),
                                       __shfl_sync(0xffffffffu, lane_nd[e / 32], e % 32 + 1));
-        const float2 ds = fmul2(make_float2(pf[e], pf[e + 1]), fadd2(dp, nd));
+        float2 pp;
+        if constexpr (kPackedP)
+          pp = make_float2(__uint_as_float(ppk[e / 2] << 16), __uint_as_float(ppk[e / 2] & 0xffff0000u));
+        else
+          pp = make_float2(pf[e], pf[e + 1]);
+        const float2 ds = fmul2(pp, fadd2(dp, nd));
         pk_ds[e / 2] = pack_bf16x2(ds.x, ds.y);
       }
       uint8_t* sDSi = sDS + (i & 1) * C::DS_TILE;
@@ -571,7 +584,9 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       for (int i = 0; ok && i < n; ++i) {
         // st_full phase i: stage i loaded, dS^T buffer i & 1 free (dK, dQ of step i-2 done)
         if (!(ok = mbar_wait(&stage_full[i % C::NST], (i / C::NST) & 1, abort_flag, 244))) break;
-        if (i >= 2 && !(ok = mbar_wait(&pds_free[i & 1], ((i >> 1) - 1) & 1, abort_flag, 245))) break;
+        if (i >= 2 && !(ok = mbar_wait(D == 128 ? &pds_free[i & 1] : &dqs_done[i & 1], ((i >> 1) - 1) & 1,
+                                       abort_flag, 245)))
+          break;
         if (i > 0 && !(ok = mbar_wait(st_full, (i - 1) & 1, abort_flag, 246))) break;
         mbar_arrive(st_full);
         if (i + 1 < n &&
@@ -627,28 +642,45 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       // the accumulator complete on their own (as a TMA store's writes do)
       if (leader) bulk_wait_group_read0();
     } else {
+      // lane = query, columns = d.  The tile is staged in the step's dS^T buffer, free once the
+      // step's dK and dQ products are done (dq_full) until the dS warps write step i+2 into it
+      // (the helper holds them until the staging has been read: dqs_done), as fp32 rows in the
+      // 128-byte-swizzled layout of two [128 x 32] TMA boxes (conflict-free 16-byte writes),
+      // then added into dQ_acc by two TMA reduce-adds issued by one thread.
+      const bool leader = threadIdx.x == 320;
+      uint32_t use = 0;
       for (int i = 0; i < n; ++i) {
         const int q0 = step_q0(i);
         const int qb = i & 1;
         if (!mbar_wait_warp(&dq_full[qb], (i >> 1) & 1, abort_flag, 231)) break;
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tbase + t_lane + C::T_DQ + qb * 64 + c * 32, v);
-          tmem_wait_ld();
-          // lane = query q0 + rr_, columns = d
-          if (q0 + rr_ < n_q) {
-            float* base = p.dq_acc + qrow(q0 + rr_) * D + c * 32;
-#pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              red_add_v4_f32(base + e, __uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                             __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-          }
-        }
+        uint32_t v[2][32];
+        tmem_ld32(tbase + t_lane + C::T_DQ + qb * 64, v[0]);
+        tmem_ld32(tbase + t_lane + C::T_DQ + qb * 64 + 32, v[1]);
+        tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&dq_free[qb]);
+        uint8_t* stg = sDS + (i & 1) * C::DS_TILE;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<float4*>(stg + h * (C::BM * 128) + rr_ * 128 + ((c ^ (rr_ & 7)) << 4)) =
+                make_float4(__uint_as_float(v[h][4 * c]), __uint_as_float(v[h][4 * c + 1]),
+                            __uint_as_float(v[h][4 * c + 2]), __uint_as_float(v[h][4 * c + 3]));
+        fence_proxy_async_smem();
+        if (!warps_sync(dqs_sync, use++ & 1, abort_flag, 234)) break;
+        if (leader) {
+          // rows past the sequence's end hold zeros (their P, hence dS, is 0); rows past the
+          // tensor are clipped
+          for (int h = 0; h < 2; ++h)
+            tma_reduce_add_3d(&p.tdq, stg + h * (C::BM * 128), h * 32, VL ? head : q0, VL ? q_beg + q0 : bh);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+          mbar_arrive(&dqs_done[i & 1]);
+        }
       }
+      if (leader) bulk_wait_group_read0();
     }
   }
 
@@ -658,6 +690,535 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// F3 persistent variant for short heads at d = 64: one CTA per SM walks (head, key tile) items,
+// rank-major (every head's first key tile, then every head's second, ...; with causal the
+// longest first) in zig-zag rounds of the grid, and runs the roles of bwd_main_kernel across
+// item boundaries.  Each mbarrier phase counts the CTA's steps (or items) from its start.  The
+// producer streams the next item's Q/dO stages while the current item finishes; K is
+// double-buffered by item and V reloaded as soon as the item's last dP product is done (it is
+// brought into L2 beforehand); the next item's first S product follows the last dV product,
+// its dP product the last dK/dQ products; and the dQ warpgroup, not the dS warps, reads dK/dV
+// out of TMEM after the item's last product and stores them row by row while the dS warps go
+// on with the next item.  Per (key tile, query step) the arithmetic, the products and their
+// order are those of bwd_main_kernel, so dK and dV agree with it bit for bit.  This removes
+// the per-CTA start (barriers, TMEM, first loads) and the dK/dV epilogue from every item but
+// the CTA's first and last, which is most of a short key tile's time.
+// ------------------------------------------------------------------------------------------
+// Key tiles per head up to which the persistent backward runs (d = 64).  Measured on GB300:
+// at 4 key tiles (512 tokens) it is 10% faster than one CTA per key tile; at 8 (a GPT-2-medium
+// layer) 2% slower and at 16 up to 15% slower: its steps run slower than bwd_main_kernel's
+// (also when launched with one CTA per item), which outweighs the per-CTA start and epilogue
+// it saves once items are longer than a few steps.
+constexpr int kPersistentBwdMaxKvTiles = 4;
+inline bool use_persistent_bwd(int n_kvtiles) { return n_kvtiles <= kPersistentBwdMaxKvTiles; }
+
+struct BwdP64 {
+  using B = BwdCfg<64>;
+  static constexpr int D = 64, BN = B::BN, BM = B::BM, NST = B::NST, HALF = B::HALF;
+  static constexpr int OFF_K = 0;                       // K of the CTA's items 2j and 2j+1
+  static constexpr int OFF_V = 2 * B::KV_TILE;
+  static constexpr int OFF_ST = 3 * B::KV_TILE;         // Q, dO ring
+  static constexpr int OFF_DS = OFF_ST + NST * B::STAGE;
+  static constexpr int OFF_LSE = OFF_DS + 2 * B::DS_TILE;
+  static constexpr int OFF_BAR = OFF_LSE + NST * B::LSE_STAGE;
+  // k_full[2], k_free[2], v_full, v_free, stage_full[NST], stage_empty[NST], st_full, dp_full,
+  // p_ready, ds_ready, pds_free[2], dq_full[2], dq_free[2], acc_full, acc_free, mma_done,
+  // dqs_sync, dqs_done[2]
+  static constexpr int NBAR = 6 + 2 * NST + 4 + 6 + 3 + 3;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // TMEM slot, abort flag
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static_assert(OFF_ST % 1024 == 0 && OFF_DS % 1024 == 0, "operands on 1 KB boundaries");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget (227 KB per CTA)");
+};
+
+// One work item of the persistent backward: key tile kt of plane bh and its query steps.
+struct BwdItem {
+  int bh, kt, i_start, n;
+};
+
+__device__ __forceinline__ BwdItem bwd_item(const BwdParams& p, int item) {
+  BwdItem it;
+  const int n_bh = p.n_items / p.n_kvtiles;
+  it.bh = item % n_bh;
+  it.kt = item / n_bh;
+  it.i_start = p.causal ? it.kt * (BwdP64::BN / BwdP64::BM) : 0;
+  it.n = max(0, p.n_qtiles - it.i_start);
+  return it;
+}
+
+__global__ void __launch_bounds__(BwdCfg<64>::THREADS, 1)
+bwd_persistent_kernel64(const __grid_constant__ BwdParams p) {
+  using C = BwdP64;
+  using B = BwdCfg<64>;
+  constexpr int D = 64;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_smem_1k(smem_raw);
+  uint8_t* sK = smem + C::OFF_K;
+  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sDS = smem + C::OFF_DS;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* k_full = bars;                 // [2] K of an item landed (one per K buffer)
+  uint64_t* k_free = k_full + 2;           // [2] the item's last product reading K is done
+  uint64_t* v_full = k_free + 2;
+  uint64_t* v_free = v_full + 1;           // the item's last dP product is done
+  uint64_t* stage_full = v_free + 1;
+  uint64_t* stage_empty = stage_full + C::NST;
+  uint64_t* st_full = stage_empty + C::NST;
+  uint64_t* dp_full = st_full + 1;
+  uint64_t* p_ready = dp_full + 1;
+  uint64_t* ds_ready = p_ready + 1;
+  uint64_t* pds_free = ds_ready + 1;       // [2]
+  uint64_t* dq_full = pds_free + 2;        // [2]
+  uint64_t* dq_free = dq_full + 2;         // [2]
+  uint64_t* acc_full = dq_free + 2;        // dK, dV of the item complete in TMEM
+  uint64_t* acc_free = acc_full + 1;       // ... and read out (the next item may overwrite)
+  uint64_t* mma_done = acc_free + 1;
+  uint64_t* dqs_sync = mma_done + 1;       // the four dQ warps around the staging
+  uint64_t* dqs_done = dqs_sync + 1;       // [2] dQ staged in dS^T buffer b read by the TMA
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = static_cast<int>(gridDim.x);
+  // the CTA's next item with work, from its c-th on; c moves past it (n = 0: none left)
+  auto next_work = [&](int& c) -> BwdItem {
+    for (;; ++c) {
+      const int item = pers_item(c, G);
+      if (item >= p.n_items) return BwdItem{0, 0, 0, 0};
+      const BwdItem it = bwd_item(p, item);
+      if (it.n > 0) {
+        ++c;
+        return it;
+      }
+    }
+  };
+  auto stage_ptr = [&](int s) { return smem + C::OFF_ST + s * B::STAGE; };
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&k_full[b], 1);
+      mbar_init(&k_free[b], 1);
+      mbar_init(&pds_free[b], 1);
+      mbar_init(&dq_full[b], 1);
+      mbar_init(&dq_free[b], 128);
+    }
+    mbar_init(v_full, 1);
+    mbar_init(v_free, 1);
+    for (int s = 0; s < C::NST; ++s) {
+      mbar_init(&stage_full[s], 2);
+      mbar_init(&stage_empty[s], 1);
+    }
+    mbar_init(st_full, 2);
+    mbar_init(dp_full, 1);
+    mbar_init(p_ready, B::DS_THREADS + 1);
+    mbar_init(ds_ready, B::DS_THREADS + 1);
+    mbar_init(acc_full, 1);
+    mbar_init(acc_free, 128);
+    mbar_init(mma_done, 1);
+    mbar_init(dqs_sync, 4);
+    mbar_init(&dqs_done[0], 1);
+    mbar_init(&dqs_done[1], 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tq);
+    tma_prefetch_desc(&p.tk);
+    tma_prefetch_desc(&p.tv);
+    tma_prefetch_desc(&p.tdo);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, B::TMEM_COLS);
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    int g = 0, j = 0, issued = 0, n_kld[2] = {0, 0}, n_vld = 0;
+    bool ok = true;
+    for (int c = 0; ok;) {
+      const BwdItem it = next_work(c);
+      if (it.n == 0) break;
+      const int kb = j & 1;
+      const int k0 = it.kt * C::BN;
+      // K of item j into buffer j & 1, free once item j - 2's last products are done
+      if (j >= 2 && !(ok = mbar_wait_warp(&k_free[kb], ((j >> 1) - 1) & 1, abort_flag, 301))) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&k_full[kb], B::KV_TILE);
+        tma_load_3d(sK + kb * B::KV_TILE, &p.tk, &k_full[kb], 0, k0, it.bh);
+        if (j > 0) tma_prefetch_l2_3d(&p.tv, 0, k0, it.bh);
+      }
+      ++n_kld[kb];
+      for (int i = 0; i < it.n; ++i, ++g) {
+        const int s = g % C::NST;
+        const uint32_t u = g / C::NST;
+        if (u > 0 && !(ok = mbar_wait_warp(&stage_empty[s], (u - 1) & 1, abort_flag, 303))) break;
+        uint8_t* st = stage_ptr(s);
+        const int q0 = (it.i_start + i) * C::BM;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&stage_full[s], 2 * B::Q_TILE);
+          tma_load_3d(st, &p.tq, &stage_full[s], 0, q0, it.bh);
+          tma_load_3d(st + B::Q_TILE, &p.tdo, &stage_full[s], 0, q0, it.bh);
+        }
+        float* s_lse = reinterpret_cast<float*>(smem + C::OFF_LSE + s * B::LSE_STAGE);
+        float* s_del = s_lse + C::BM;
+        for (int e = lane; e < C::BM; e += 32) {
+          const int q = q0 + e;
+          const size_t li = static_cast<size_t>(it.bh) * p.n_q + q;
+          s_lse[e] = (q < p.n_q) ? -p.lse[li] * 1.4426950408889634f : -INFINITY;
+          s_del[e] = (q < p.n_q) ? -p.delta[li] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&stage_full[s]);
+        issued = g + 1;
+        if (i == 0) {
+          // V of item j, once item j - 1's last dP product is done with the buffer
+          if (j >= 1 && !(ok = mbar_wait_warp(v_free, (j - 1) & 1, abort_flag, 302))) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(v_full, B::KV_TILE);
+            tma_load_3d(sV, &p.tv, v_full, 0, k0, it.bh);
+          }
+          ++n_vld;
+        }
+      }
+      ++j;
+    }
+    if (!ok && lane == 0) {
+      // loads still in flight land in this CTA's shared memory: let them finish first
+      for (int b = 0; b < 2; ++b)
+        if (n_kld[b] > 0) mbar_wait(&k_full[b], (n_kld[b] - 1) & 1, nullptr, 304);
+      if (n_vld > 0) mbar_wait(v_full, (n_vld - 1) & 1, nullptr, 305);
+      for (int g2 = max(0, issued - C::NST); g2 < issued; ++g2)
+        mbar_wait(&stage_full[g2 % C::NST], (g2 / C::NST) & 1, nullptr, 306);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(128, C::BM, 0, 0);
+      const uint32_t id_acc = idesc_bf16_f32(128, D, 0, 1);
+      const uint32_t id_dq = idesc_bf16_f32(128, 64, 1, 1);
+      const uint64_t dK_k = smem_desc_sw128(smem_u32(sK), 0, 1024);
+      const uint64_t dV_k = smem_desc_sw128(smem_u32(sV), 0, 1024);
+      const uint64_t dK_mn = smem_desc_sw128(smem_u32(sK), B::KV_CHUNK, 1024);
+      const uint64_t dDS = smem_desc_sw128(smem_u32(sDS), 0, 1024);
+      const uint64_t dDS_mn = smem_desc_sw128(smem_u32(sDS), B::KV_CHUNK, 1024);
+      const uint64_t dST_k = smem_desc_sw128(smem_u32(stage_ptr(0)), 0, 1024);
+      const uint64_t dST_mn = smem_desc_sw128(smem_u32(stage_ptr(0)), B::Q_CHUNK, 1024);
+      auto issue_s = [&](int g, int kb) {
+        const uint64_t q_k = desc_advance(dST_k, (g % C::NST) * B::STAGE);
+        const uint64_t k_k = desc_advance(dK_k, kb * B::KV_TILE);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma_ss(tbase + B::T_S, desc_advance(k_k, ks * 32), desc_advance(q_k, ks * 32), id_s, ks > 0);
+        umma_commit(st_full);
+      };
+      auto issue_dp = [&](int g, bool item_last) {
+        const uint64_t do_k = desc_advance(dST_k, (g % C::NST) * B::STAGE + B::Q_TILE);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma_ss(tbase + B::T_DP, desc_advance(dV_k, ks * 32), desc_advance(do_k, ks * 32), id_s, ks > 0);
+        umma_commit(dp_full);
+        if (item_last) umma_commit(v_free);
+      };
+      int c = 0;
+      BwdItem cur = next_work(c);
+      bool ok = true;
+      if (cur.n > 0) {
+        ok = mbar_wait(&k_full[0], 0, abort_flag, 311) && mbar_wait(v_full, 0, abort_flag, 312) &&
+             mbar_wait(&stage_full[0], 0, abort_flag, 313);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0, 0);
+          issue_dp(0, cur.n == 1);
+        }
+      }
+      unsigned long long steps = 0;
+      int g = 0;
+      for (int j = 0; ok && cur.n > 0; ++j) {
+        const BwdItem nxt = next_work(c);
+        const int kb = j & 1;
+        const uint64_t k_mn = desc_advance(dK_mn, kb * B::KV_TILE);
+        for (int i = 0; i < cur.n; ++i, ++g) {
+          const int s = g % C::NST;
+          // p_ready(g) folds in: stage g+1 loaded, the next item's K (at its boundary), and
+          // dK/dV of the previous item read out (at an item's first step)
+          if (!(ok = mbar_wait(p_ready, g & 1, abort_flag, 315))) break;
+          tc_fence_after();
+          const uint64_t q_mn = desc_advance(dST_mn, s * B::STAGE);
+          const uint64_t do_mn = desc_advance(dST_mn, s * B::STAGE + B::Q_TILE);
+#pragma unroll
+          for (int ks = 0; ks < C::BM / 16; ++ks)       // dV += P^T dO
+            umma_ts(tbase + B::T_DV, tbase + B::T_S + ks * 8 + ((16 * ks) / C::HALF) * (C::HALF / 2),
+                    desc_advance(do_mn, ks * 2048), id_acc, (i > 0 || ks > 0) ? 1u : 0u);
+          if (i + 1 < cur.n) {
+            issue_s(g + 1, kb);
+            issue_dp(g + 1, i + 2 == cur.n);
+          } else if (nxt.n > 0) {
+            issue_s(g + 1, kb ^ 1);                     // dP of the next item after dK/dQ below
+          }
+          if (!(ok = mbar_wait(ds_ready, g & 1, abort_flag, 318))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < C::BM / 16; ++ks) {     // dK += dS^T Q
+            const uint32_t a_off = (ks >> 2) * B::KV_CHUNK + (ks & 3) * 32;
+            umma_ss(tbase + B::T_DK, desc_advance(dDS, (g & 1) * B::DS_TILE + a_off),
+                    desc_advance(q_mn, ks * 2048), id_acc, (i > 0 || ks > 0) ? 1u : 0u);
+          }
+          const int qb = g & 1;
+#pragma unroll
+          for (int ks = 0; ks < C::BN / 16; ++ks)       // dQ = dS K
+            umma_ss(tbase + B::T_DQ + qb * 64, desc_advance(dDS_mn, (g & 1) * B::DS_TILE + ks * 2048),
+                    desc_advance(k_mn, ks * 2048), id_dq, ks > 0);
+          umma_commit(&dq_full[qb]);
+          umma_commit(&pds_free[g & 1]);
+          umma_commit(&stage_empty[s]);
+          ++steps;
+          if (i + 1 == cur.n) {
+            umma_commit(&k_free[kb]);
+            umma_commit(acc_full);
+            if (nxt.n > 0) {
+              // the next item's V: reloaded once this item's last dP product was done
+              if (!(ok = mbar_wait(v_full, (j + 1) & 1, abort_flag, 319))) break;
+              tc_fence_after();
+              issue_dp(g + 1, nxt.n == 1);
+            }
+          }
+        }
+        cur = nxt;
+      }
+      umma_commit(mma_done);
+      mbar_wait(mma_done, 0, nullptr, 317);
+      if (ok && p.stats != nullptr) atomicAdd(&p.stats[1], steps);
+    }
+  } else if (warp < 10) {
+    // ------------------------------------------------------------------ dS warpgroups
+    // (the step of bwd_main_kernel without window or block mask)
+    const int sub = warp & 3;
+    const int grp = (warp - 2) >> 2;
+    const int cb = grp * C::HALF;
+    const int r = sub * 32 + lane;
+    const uint32_t t_lane = static_cast<uint32_t>(sub * 32) << 16;
+    const float c2 = p.scale_log2;
+    const float2 c2v = make_float2(c2, c2);
+    bool ok = true;
+    int g = 0;
+    for (int c = 0; ok;) {
+      const BwdItem it = next_work(c);
+      if (it.n == 0) break;
+      const int k0 = it.kt * C::BN;
+      const int k_idx = k0 + r;
+      const bool row_dead = k_idx >= p.n_kv;
+      for (int i = 0; i < it.n; ++i, ++g) {
+        const int q0 = (it.i_start + i) * C::BM;
+        if (!(ok = mbar_wait_warp(&stage_full[g % C::NST], (g / C::NST) & 1, abort_flag, 325))) break;
+        const float* s_nlse = reinterpret_cast<const float*>(smem + C::OFF_LSE + (g % C::NST) * B::LSE_STAGE);
+        const float* s_nd = s_nlse + C::BM;
+        float lane_nd[C::HALF / 32], nl0[32];
+        {
+          const float lane_nl = s_nlse[cb + lane];
+          lane_nd[0] = s_nd[cb + lane];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) nl0[e] = __shfl_sync(0xffffffffu, lane_nl, e);
+        }
+        if (!(ok = mbar_wait_warp(st_full, g & 1, abort_flag, 321))) break;
+        tc_fence_after();
+        const bool diag = p.causal && (q0 < k0 + C::BN - 1);
+        uint32_t pk_ds[C::HALF / 2];
+        uint32_t ppk[C::HALF / 2];                   // P as bf16 pairs (see bwd_main_kernel)
+        uint32_t dpu[C::HALF / 32][32];
+#pragma unroll
+        for (int cc = 0; cc < C::HALF / 32; ++cc) {
+          uint32_t rs[32];
+          tmem_ld32(tbase + t_lane + B::T_S + cb + cc * 32, rs);
+          float nl[32];
+          if (cc == 0) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) nl[e] = nl0[e];
+          } else {
+            const float lane_nl = s_nlse[cb + cc * 32 + lane];
+            lane_nd[cc] = s_nd[cb + cc * 32 + lane];
+#pragma unroll
+            for (int e = 0; e < 32; ++e) nl[e] = __shfl_sync(0xffffffffu, lane_nl, e);
+          }
+          tmem_wait_ld();
+          uint32_t pk_p[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int col = cb + cc * 32 + e;
+            const float2 x = ffma2(make_float2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2v,
+                                   make_float2(nl[e], nl[e + 1]));
+            float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+            if (row_dead || (diag && k_idx > q0 + col)) p0 = 0.f;
+            if (row_dead || (diag && k_idx > q0 + col + 1)) p1 = 0.f;
+            pk_p[e / 2] = pack_bf16x2(p0, p1);
+            ppk[cc * 16 + e / 2] = pk_p[e / 2];
+          }
+          tmem_st16(tbase + t_lane + B::T_S + cb + cc * 16, pk_p);
+        }
+        if (!(ok = mbar_wait_warp(dp_full, g & 1, abort_flag, 324))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < C::HALF / 32; ++cc) tmem_ld32(tbase + t_lane + B::T_DP + cb + cc * 32, dpu[cc]);
+        tmem_wait_ld();
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_ready);
+#pragma unroll
+        for (int e = 0; e < C::HALF; e += 2) {
+          const float2 dp = make_float2(__uint_as_float(dpu[e / 32][e % 32]), __uint_as_float(dpu[e / 32][e % 32 + 1]));
+          const float2 nd = make_float2(__shfl_sync(0xffffffffu, lane_nd[e / 32], e % 32),
+                                        __shfl_sync(0xffffffffu, lane_nd[e / 32], e % 32 + 1));
+          const float2 pp = make_float2(__uint_as_float(ppk[e / 2] << 16), __uint_as_float(ppk[e / 2] & 0xffff0000u));
+          const float2 ds = fmul2(pp, fadd2(dp, nd));
+          pk_ds[e / 2] = pack_bf16x2(ds.x, ds.y);
+        }
+        uint8_t* sDSi = sDS + (g & 1) * B::DS_TILE;
+#pragma unroll
+        for (int u = 0; u < C::HALF / 8; ++u) {
+          const int c8 = cb / 8 + u;
+          const uint32_t off = (c8 >> 3) * B::KV_CHUNK + sw128_offset(r, (c8 & 7) * 8);
+          *reinterpret_cast<uint4*>(sDSi + off) =
+              make_uint4(pk_ds[4 * u], pk_ds[4 * u + 1], pk_ds[4 * u + 2], pk_ds[4 * u + 3]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(ds_ready);
+      }
+    }
+  } else if (warp == 14) {
+    // ------------------------------------------------------------------ helper
+    // As in bwd_main_kernel, plus the item boundaries: p_ready of an item's last step also
+    // waits for the next item's K (its first S product follows that step's dV), and p_ready of
+    // an item's first step for the previous item's dK/dV to be read out of TMEM (that step's
+    // dV and dK products start the accumulators afresh).
+    if (lane == 0) {
+      int c = 0, g = 0;
+      BwdItem cur = next_work(c);
+      bool ok = cur.n == 0 || mbar_wait(&k_full[0], 0, abort_flag, 340);
+      for (int j = 0; ok && cur.n > 0; ++j) {
+        const BwdItem nxt = next_work(c);
+        for (int i = 0; i < cur.n; ++i, ++g) {
+          const bool last = i + 1 == cur.n;
+          const bool more = !last || nxt.n > 0;
+          if (!(ok = mbar_wait(&stage_full[g % C::NST], (g / C::NST) & 1, abort_flag, 344))) break;
+          if (g >= 2 && !(ok = mbar_wait(&dqs_done[g & 1], ((g >> 1) - 1) & 1, abort_flag, 345))) break;
+          if (g > 0 && !(ok = mbar_wait(st_full, (g - 1) & 1, abort_flag, 346))) break;
+          mbar_arrive(st_full);
+          if (more && !(ok = mbar_wait(&stage_full[(g + 1) % C::NST], ((g + 1) / C::NST) & 1, abort_flag, 341)))
+            break;
+          if (last && nxt.n > 0 && !(ok = mbar_wait(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1, abort_flag, 347)))
+            break;
+          if (i == 0 && j > 0 && !(ok = mbar_wait(acc_free, (j - 1) & 1, abort_flag, 348))) break;
+          if (g > 0 && !(ok = mbar_wait(p_ready, (g - 1) & 1, abort_flag, 342))) break;
+          mbar_arrive(p_ready);
+          if (g >= 2 && !(ok = mbar_wait(&dq_free[g & 1], ((g >> 1) - 1) & 1, abort_flag, 343))) break;
+          if (g > 0 && !(ok = mbar_wait(ds_ready, (g - 1) & 1, abort_flag, 349))) break;
+          mbar_arrive(ds_ready);
+        }
+        cur = nxt;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------------ dQ warpgroup
+    // Per step: dQ (lane = query, columns = d) from TMEM into the fp32 accumulator, staged in the
+    // step's dS^T buffer and added by two TMA reduce-adds (as in bwd_main_kernel at d = 64).
+    // Per item, once its last products are done: first dK (times scale) and dV
+    // (lane = key row) out of TMEM and the accumulators released (the next item's first dV
+    // product waits for that), stored row by row as bf16 (zeros for a key tile no query sees);
+    // then the last step's dQ.
+    const int sub = warp & 3;
+    const int rr_ = sub * 32 + lane;
+    const uint32_t t_lane = static_cast<uint32_t>(sub * 32) << 16;
+    const bool leader = threadIdx.x == 320;
+    uint32_t use = 0;                                // dqs_sync phases used so far
+    bool ok = true;
+    int g = 0, j = 0;
+    auto store_dk_dv = [&](const BwdItem& it) {
+      const int k_idx = it.kt * C::BN + rr_;
+      const bool live = k_idx < p.n_kv;
+      const size_t row = (static_cast<size_t>(it.bh) * p.n_kv + (live ? k_idx : 0)) * D;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {                // dV, then dK (times scale)
+        const float mul = t ? p.scale : 1.f;
+        uint4* dst = reinterpret_cast<uint4*>((t ? p.dk : p.dv) + row);
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t v[32];
+          if (it.n > 0) {
+            tmem_ld32(tbase + t_lane + (t ? B::T_DK : B::T_DV) + cc * 32, v);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = 0u;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            pk[e / 2] = pack_bf16x2(__uint_as_float(v[e]) * mul, __uint_as_float(v[e + 1]) * mul);
+          if (live) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              dst[cc * 4 + u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+          }
+        }
+      }
+    };
+    for (int c = 0; ok; ++c) {
+      const int item = pers_item(c, G);
+      if (item >= p.n_items) break;
+      const BwdItem it = bwd_item(p, item);
+      if (it.n == 0) store_dk_dv(it);
+      for (int i = 0; i < it.n; ++i, ++g) {
+        const int q0 = (it.i_start + i) * C::BM;
+        const int qb = g & 1;
+        if (i + 1 == it.n) {
+          // acc_full(j) is committed after this step's dQ product: it covers dq_full too
+          if (!(ok = mbar_wait_warp(acc_full, j & 1, abort_flag, 332))) break;
+          tc_fence_after();
+          store_dk_dv(it);
+          tc_fence_before();
+          mbar_arrive(acc_free);
+          ++j;
+        }
+        if (!(ok = mbar_wait_warp(&dq_full[qb], (g >> 1) & 1, abort_flag, 331))) break;
+        tc_fence_after();
+        uint32_t v[2][32];
+        tmem_ld32(tbase + t_lane + B::T_DQ + qb * 64, v[0]);
+        tmem_ld32(tbase + t_lane + B::T_DQ + qb * 64 + 32, v[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&dq_free[qb]);
+        uint8_t* stg = sDS + (g & 1) * B::DS_TILE;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc)
+            *reinterpret_cast<float4*>(stg + h * (C::BM * 128) + rr_ * 128 + ((cc ^ (rr_ & 7)) << 4)) =
+                make_float4(__uint_as_float(v[h][4 * cc]), __uint_as_float(v[h][4 * cc + 1]),
+                            __uint_as_float(v[h][4 * cc + 2]), __uint_as_float(v[h][4 * cc + 3]));
+        fence_proxy_async_smem();
+        if (!(ok = warps_sync(dqs_sync, use++ & 1, abort_flag, 333))) break;
+        if (leader) {
+          for (int h = 0; h < 2; ++h) tma_reduce_add_3d(&p.tdq, stg + h * (C::BM * 128), h * 32, q0, it.bh);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+          mbar_arrive(&dqs_done[g & 1]);
+        }
+      }
+    }
+    if (leader) bulk_wait_group_read0();
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, B::TMEM_COLS);
   }
 }
 
@@ -732,7 +1293,7 @@ static cudaError_t launch_bwd_main_d(const BwdArgs& a, cudaStream_t stream) {
   const uint64_t nq = a.n_q > 0 ? a.n_q : 1;
   const void* qb = a.n_q > 0 ? a.q : a.k;
   const void* dob = a.n_q > 0 ? a.dO : a.k;
-  if ((D == 128 && !make_map_f32_3d(&p.tdq, a.dq_acc, D, nq, bh, D * 4, D * 4 * nq, D, C::BM, 1)) ||
+  if (!make_map_f32_3d(&p.tdq, a.dq_acc, D, nq, bh, D * 4, D * 4 * nq, D == 128 ? D : 32, C::BM, 1, D == 64) ||
       !make_map_bf16_3d(&p.tq, qb, D, nq, bh, 64, C::BM) ||
       !make_map_bf16_3d(&p.tdo, dob, D, nq, bh, 64, C::BM) ||
       !make_map_bf16_3d(&p.tk, a.k, D, a.n_kv, bh, 64, C::BN) ||
@@ -760,6 +1321,7 @@ static cudaError_t launch_bwd_main_d(const BwdArgs& a, cudaStream_t stream) {
   p.block_mask = a.block_mask;
   p.bm_per_head = a.bm_per_head;
   p.n_qblocks = (a.n_q + kBlockSize - 1) / kBlockSize;
+  p.n_items = 0;
   static int attr_done[64] = {0};   // one per instantiation of this launcher
   const uint64_t grid = static_cast<uint64_t>(p.n_kvtiles) * bh;
   if (a.block_mask != nullptr) {
@@ -769,6 +1331,21 @@ static cudaError_t launch_bwd_main_d(const BwdArgs& a, cudaStream_t stream) {
     log_launch("bwd_main_kernel<D, false, false, true>", static_cast<unsigned long long>(static_cast<unsigned>(grid)), C::THREADS, static_cast<unsigned long long>(C::SMEM_BYTES));
     bwd_main_kernel<D, false, false, true><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
+  }
+  if constexpr (D == 64) {
+    if (!a.windowed && use_persistent_bwd(p.n_kvtiles)) {
+      static int attr_p[64] = {0};
+      cudaError_t e = ensure_smem_attr(bwd_persistent_kernel64, BwdP64::SMEM_BYTES, attr_p);
+      if (e != cudaSuccess) return e;
+      int dev = 0, sms = 0;
+      if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+      if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+      p.n_items = static_cast<int>(grid);
+      const unsigned ctas = static_cast<unsigned>(std::min<uint64_t>(grid, static_cast<uint64_t>(std::max(sms, 1))));
+      log_launch("bwd_persistent_kernel64", static_cast<unsigned long long>(ctas), C::THREADS, static_cast<unsigned long long>(BwdP64::SMEM_BYTES));
+      bwd_persistent_kernel64<<<ctas, C::THREADS, BwdP64::SMEM_BYTES, stream>>>(p);
+      return cudaGetLastError();
+    }
   }
   if (a.windowed) {
     static int attr_win[64] = {0};
@@ -794,8 +1371,8 @@ static cudaError_t launch_bwd_main_varlen_d(const BwdArgs& a, cudaStream_t strea
   const int tq = a.total_q > 0 ? a.total_q : 1;
   const void* qb = a.total_q > 0 ? a.q : a.k;
   const void* dob = a.total_q > 0 ? a.dO : a.k;
-  if ((D == 128 && !make_map_f32_3d(&p.tdq, a.dq_acc, D, a.H, tq, D * 4, static_cast<uint64_t>(D) * 4 * a.H,
-                                    D, 1, C::BM)) ||
+  if (!make_map_f32_3d(&p.tdq, a.dq_acc, D, a.H, tq, D * 4, static_cast<uint64_t>(D) * 4 * a.H,
+                       D == 128 ? D : 32, 1, C::BM, D == 64) ||
       !make_map_bf16_tok(&p.tq, qb, D, a.H, tq, 64, C::BM) ||
       !make_map_bf16_tok(&p.tdo, dob, D, a.H, tq, 64, C::BM) ||
       !make_map_bf16_tok(&p.tk, a.k, D, a.H, a.total_k, 64, C::BN) ||
@@ -825,6 +1402,7 @@ static cudaError_t launch_bwd_main_varlen_d(const BwdArgs& a, cudaStream_t strea
   attention_window(a.causal, false, 0, 0, &p.win_left, &p.win_right);
   p.block_mask = nullptr;
   p.bm_per_head = p.n_qblocks = 0;
+  p.n_items = 0;
   static int attr_done[64] = {0};
   cudaError_t e = ensure_smem_attr(bwd_main_kernel<D, true>, C::SMEM_BYTES, attr_done);
   if (e != cudaSuccess) return e;

@@ -51,6 +51,12 @@ __device__ __forceinline__ void causal_item(int block, int n_bh, int per_head, i
   *bh = g0 + w % g;
 }
 
+// Item k of a persistent CTA: rounds of gridDim.x items, walked forward in even rounds and
+// backward in odd ones, so that with items ordered longest first every CTA gets a similar total.
+__device__ __forceinline__ int pers_item(int k, int G) {
+  return k * G + ((k & 1) ? G - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
+}
+
 // Window of a call: an explicit window (win_left / win_right >= 0 or kWinUnbounded) when
 // ``windowed``, else causal = (unbounded, 0) or no mask = (unbounded, unbounded).
 inline void attention_window(int causal, bool windowed, int left, int right, int* wl, int* wr) {

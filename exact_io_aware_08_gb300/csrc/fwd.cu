@@ -823,12 +823,6 @@ struct FwdItem {
   int bh, q0[2], n_t[2], n_max;
 };
 
-// Item k of this CTA: rounds of gridDim.x items, walked forward in even rounds and backward in
-// odd ones, so that with items ordered longest first every CTA gets a similar total.
-__device__ __forceinline__ int pers_item(int k, int G) {
-  return k * G + ((k & 1) ? G - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
-}
-
 __device__ __forceinline__ FwdItem fwd_item(const FwdParams& p, int item) {
   FwdItem it;
   // rank-major: every head's longest item (causal), then every head's second, ...; the short

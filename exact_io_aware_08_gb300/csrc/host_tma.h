@@ -79,9 +79,10 @@ inline bool make_map_bf16_tok(CUtensorMap* map, const void* base, uint64_t d, ui
 
 // fp32 tensor {d0, d1, d2} with byte strides (stride1, stride2) for dims 1 and 2; box
 // {b0, b1, b2}; no swizzle (a row-major box in shared memory).
+// ``sw128``: the shared-memory box uses the 128-byte swizzle (inner box extent 32 floats).
 inline bool make_map_f32_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1,
                             uint64_t d2, uint64_t stride1, uint64_t stride2, uint32_t b0,
-                            uint32_t b1, uint32_t b2) {
+                            uint32_t b1, uint32_t b2, bool sw128 = false) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   const cuuint64_t dims[3] = {d0, d1, d2};
@@ -89,7 +90,8 @@ inline bool make_map_f32_3d(CUtensorMap* map, const void* base, uint64_t d0, uin
   const cuuint32_t box[3] = {b0, b1, b2};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }

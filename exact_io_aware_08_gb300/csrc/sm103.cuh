@@ -190,6 +190,12 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
+// 3-D tile brought into L2 ahead of a later load (no destination, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+               :: "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2) : "memory");
+}
+
 // 3-D tile store from shared memory (rows outside the tensor are not written).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src,
                                              int c0, int c1, int c2) {

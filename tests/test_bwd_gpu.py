@@ -42,6 +42,7 @@ SHAPES = [
     (1, 1, 640, 640, 64, True),
     (3, 4, 700, 700, 128, True),     # 12 heads: causal items ordered across a full and a partial group
     (3, 3, 300, 300, 64, True),      # 9 heads, d = 64
+    (1, 2, 77, 1000, 64, False),
 ]
 
 
@@ -114,6 +115,33 @@ def test_bwd_headline_workload_sampled(w):
 def test_bwd_long_workload_with_outliers_sampled():
     require_gpu()
     _sampled_heads(inputs.LONG, heads=[0, 15], n_rows=24)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [300, 512])
+def test_bwd_short_heads_many_items_per_cta(causal, N):
+    """Short heads at d = 64 (up to 4 key tiles) run on the persistent backward, each CTA taking
+    several (head, key tile) items (4 x 32 heads x 3 or 4 key tiles): dK and dV must agree bit
+    for bit with the one-CTA-per-tile kernel (which the windowed entry point runs for the same
+    mask), dQ (summed across key tiles in a run-dependent order) within the tolerance, and all
+    three with the oracle on sampled heads."""
+    require_gpu()
+    B, H, d = 4, 32, 64
+    scale = d ** -0.5
+    x = inputs.make_qkv(B, H, N, N, d, seed=61 + N)
+    q, k, v, do = (cuda(x[n]) for n in ("q", "k", "v", "do"))
+    o, lse = fa.forward(q, k, v, causal=causal, scale=scale)
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, causal=causal, scale=scale)
+    dq_w, dk_w, dv_w = fa.backward_window(q, k, v, o, lse, do, -1, 0 if causal else -1, scale=scale)
+    fa.fa_sync_status()
+    assert torch.equal(dk, dk_w) and torch.equal(dv, dv_w)
+    assert_grad_close(dq, dq_w.double().cpu().numpy(), "dQ")
+    for b, h in ((0, 0), (1, 13), (3, 31)):
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        rq, rk, rv, _ = A.backward(x["q"][sl], x["k"][sl], x["v"][sl], x["do"][sl], scale, causal)
+        assert_grad_close(dq[sl], rq, "dQ")
+        assert_grad_close(dk[sl], rk, "dK")
+        assert_grad_close(dv[sl], rv, "dV")
 
 
 def test_bwd_dk_dv_deterministic():
