@@ -132,7 +132,7 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
   uint64_t* dp_full = st_full + 1;       // dP^T of the step is in TMEM (committed after S^T)
   uint64_t* p_ready = dp_full + 1;       // P^T of the step is in TMEM (dV may start)
   uint64_t* ds_ready = p_ready + 1;      // dS^T of the step is in shared memory (dK, dQ may start)
-  uint64_t* pds_free = ds_ready + 1;     // [2], one per dS^T buffer
+  uint64_t* pds_free = ds_ready + 1;     // [2], one per dS^T buffer (d = 128)
   uint64_t* dq_full = pds_free + 2;      // [2], one per dQ TMEM buffer
   uint64_t* dq_free = dq_full + 2;       // [2]
   uint64_t* mma_done = dq_free + 2;
@@ -396,7 +396,7 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
           else umma_ss(tbase + C::T_DQ + qb * 64, dd, kd, id_dq, ks > 0);
         }
         umma_commit(&dq_full[qb]);
-        umma_commit(&pds_free[i & 1]);
+        if constexpr (D == 128) umma_commit(&pds_free[i & 1]);   // d = 64: dqs_done (dQ warps)
         umma_commit(&stage_empty[s]);
       }
       umma_commit(mma_done);
@@ -735,9 +735,9 @@ struct BwdP64 {
   static constexpr int OFF_LSE = OFF_DS + 2 * B::DS_TILE;
   static constexpr int OFF_BAR = OFF_LSE + NST * B::LSE_STAGE;
   // k_full[2], k_free[2], v_full, v_free, stage_full[NST], stage_empty[NST], st_full, dp_full,
-  // p_ready, ds_ready, pds_free[2], dq_full[2], dq_free[2], acc_full, acc_free, mma_done,
-  // dqs_sync, dqs_done[2]
-  static constexpr int NBAR = 6 + 2 * NST + 4 + 6 + 3 + 3;
+  // p_ready, ds_ready, dq_full[2], dq_free[2], acc_full, acc_free, mma_done, dqs_sync,
+  // dqs_done[2]
+  static constexpr int NBAR = 6 + 2 * NST + 4 + 4 + 3 + 3;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // TMEM slot, abort flag
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static_assert(OFF_ST % 1024 == 0 && OFF_DS % 1024 == 0, "operands on 1 KB boundaries");
@@ -780,8 +780,7 @@ bwd_persistent_kernel64(const __grid_constant__ BwdParams p) {
   uint64_t* dp_full = st_full + 1;
   uint64_t* p_ready = dp_full + 1;
   uint64_t* ds_ready = p_ready + 1;
-  uint64_t* pds_free = ds_ready + 1;       // [2]
-  uint64_t* dq_full = pds_free + 2;        // [2]
+  uint64_t* dq_full = ds_ready + 1;        // [2]
   uint64_t* dq_free = dq_full + 2;         // [2]
   uint64_t* acc_full = dq_free + 2;        // dK, dV of the item complete in TMEM
   uint64_t* acc_free = acc_full + 1;       // ... and read out (the next item may overwrite)
@@ -812,7 +811,6 @@ bwd_persistent_kernel64(const __grid_constant__ BwdParams p) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(&k_full[b], 1);
       mbar_init(&k_free[b], 1);
-      mbar_init(&pds_free[b], 1);
       mbar_init(&dq_full[b], 1);
       mbar_init(&dq_free[b], 128);
     }
@@ -984,7 +982,6 @@ bwd_persistent_kernel64(const __grid_constant__ BwdParams p) {
             umma_ss(tbase + B::T_DQ + qb * 64, desc_advance(dDS_mn, (g & 1) * B::DS_TILE + ks * 2048),
                     desc_advance(k_mn, ks * 2048), id_dq, ks > 0);
           umma_commit(&dq_full[qb]);
-          umma_commit(&pds_free[g & 1]);
           umma_commit(&stage_empty[s]);
           ++steps;
           if (i + 1 == cur.n) {

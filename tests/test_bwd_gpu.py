@@ -144,6 +144,24 @@ def test_bwd_short_heads_many_items_per_cta(causal, N):
         assert_grad_close(dv[sl], rv, "dV")
 
 
+@pytest.mark.parametrize("d,nkv", [(64, 300), (64, 1500), (128, 700)])
+def test_bwd_without_queries_gives_zero_dk_dv(d, nkv):
+    """N_q = 0: no query sees any key, so dK = dV = 0 everywhere (the persistent backward at
+    d = 64 with 3 key tiles, bwd_main_kernel otherwise); outputs start as NaN so an unwritten
+    element fails."""
+    require_gpu()
+    g = torch.Generator().manual_seed(40 + d)
+    k, v = (cuda(torch.randn(2, 3, nkv, d, generator=g).to(torch.bfloat16)) for _ in range(2))
+    q = torch.empty(2, 3, 0, d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(2, 3, 0, dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(fa.fa_bwd_workspace_size(2, 3, 0, nkv, d), 256), dtype=torch.uint8,
+                     device="cuda")
+    dk, dv = poisoned(k.shape, torch.bfloat16), poisoned(v.shape, torch.bfloat16)
+    fa.fa_bwd(q, k, v, q, lse, q, q, dk, dv, ws, d ** -0.5, False)
+    fa.fa_sync_status()
+    assert (dk.float() == 0).all() and (dv.float() == 0).all()
+
+
 def test_bwd_dk_dv_deterministic():
     require_gpu()
     x = inputs.make_qkv(1, 2, 512, 512, 128, seed=5)
