@@ -154,9 +154,17 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
   // of kCausalGroup heads.
   // Variable-length: item = (sequence, head, 256-row block), sized by the longest sequence;
   // blocks past a sequence's end exit at once.  Rows are then local to the sequence.
+  // Under a block mask every head's rank-0 item runs first, then every head's rank 1, ...: the
+  // work of an item is its rows' set blocks, so the heads' longest items start together instead
+  // of the last head group's starting late (as in the block-sparse backward).
   int bh = blockIdx.x / p.n_qpairs;                   // fixed length: (b, h) plane
   int r = blockIdx.x % p.n_qpairs;
-  if (!VL && !WIN && p.causal) causal_item(blockIdx.x, gridDim.x / p.n_qpairs, p.n_qpairs, &bh, &r);
+  if (BS) {
+    bh = blockIdx.x % (gridDim.x / p.n_qpairs);
+    r = blockIdx.x / (gridDim.x / p.n_qpairs);
+  } else if (!VL && !WIN && p.causal) {
+    causal_item(blockIdx.x, gridDim.x / p.n_qpairs, p.n_qpairs, &bh, &r);
+  }
   int n_q = p.n_q, n_kv = p.n_kv, q_beg = 0, k_beg = 0, head = 0;
   if (VL) {
     const int seq = bh / p.heads;
