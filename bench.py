@@ -11,20 +11,27 @@ Also measured in the same run and reported in the same JSON line:
   breakdown.*_causal       the causal variant of the workload
   breakdown.decode         split-KV decode (B=64, H=32, N_kv=32768, d=128, 64 splits), GB/s
   breakdown.decode_paged   the same decode over a paged cache (256-key blocks, shuffled), GB/s
-  breakdown.fwd_fp8*       forward from e4m3 Q, K, V (per-tensor scales), same shapes
-  breakdown.gpt2m_*        a GPT-2-medium attention layer, 8x16x1024x64 causal, fwd and fwd+bwd
+  breakdown.fwd_fp8*       forward from e4m3 Q, K, V (per-tensor scales), same shapes; the
+                           fraction is of the fp8 GEMM rate measured in the same run
+  breakdown.gemm_peaks     dense 8192^3 GEMM rates measured here (torch.matmul bf16 and
+                           torch._scaled_mm e4m3, best of 10): the fp8 denominator
+  breakdown.gpt2m_*        a GPT-2-medium attention layer, 8x16x1024x64 causal, fwd and fwd+bwd;
+                           its inputs fit in L2, so a 256 MB buffer is written before every
+                           timed call; per-call CUDA events
   breakdown.long_*         1x16x16384x128 causal with outlier keys, fwd and fwd+bwd
   breakdown.window         forward and forward+backward under a 4096-key causal sliding window
-                           on 1x16x16384x128
+                           (left 4095, right 0) on 1x16x16384x128
   breakdown.block_sparse   the same shape under a causal 128x128 block pattern (a band of one
-                           block, the first key block, 5% random blocks)
-  breakdown.varlen         a packed batch of 16 causal sequences of 512..8192 tokens (H=32,
-                           d=128), forward and forward+backward
+                           block, the first key block, 5% random blocks; ``density`` = share of
+                           blocks set); FLOP = 4 d (fwd), 10 d (bwd) per visible pair
+  breakdown.varlen         a packed batch of 16 causal sequences of 512..8192 tokens (seed
+                           1006, H=32, d=128), forward and forward+backward
   roofline                 the dominant kernel of the step (backward main kernel), timed alone
   e2e                      the step through the public Python API with host (pinned) buffers,
                            host->device and device->host copies inside the timed region
   cpu_baseline             the fp64 oracle on a bounded sample, on this machine's host cores
   clocks                   nvidia-smi samples taken while the timed regions ran
+  summary                  (last key of the line) [rate, fraction of measured peak] per workload
 
 ``--impl reference`` times the fp64 CPU oracle instead (the reference arm for this build).
 
@@ -234,6 +241,74 @@ def time_oracle(w, budget_s: float = 12.0, max_heads: int = 8):
     }
 
 
+def summarize(bd, peak_tf):
+    """Compact per-workload figures: [TFLOP/s (GB/s for decode), fraction of its peak]."""
+    def pair(rate, frac):
+        return [rate, None if frac is None else round(frac, 3)]
+
+    def tf(name, key="tflops"):
+        e = bd.get(name) or {}
+        v = e.get(key)
+        return pair(v, None if v is None else v / peak_tf)
+    out = {"unit": "[TFLOP/s or GB/s, frac of measured peak]",
+           "fwd": pair(bd["fwd"]["tflops"], bd["fwd"]["frac_of_peak"]),
+           "fwd_bwd": tf("fwd_bwd"), "fwd_causal": tf("fwd_causal"), "fwd_bwd_causal": tf("fwd_bwd_causal")}
+    for name in ("gpt2m_8x16x1024x64_causal", "long_1x16x16384x128_causal_outliers"):
+        e = bd.get(name)
+        if e:
+            short = "gpt2m" if name.startswith("gpt2m") else "long"
+            out[short + "_fwd"] = pair(e["fwd_tflops"], e.get("fwd_frac"))
+            out[short + "_fwd_bwd"] = pair(e["fwd_bwd_tflops"], e.get("fwd_bwd_frac"))
+    for name in ("window", "block_sparse", "varlen"):
+        if name in bd:
+            out[name + "_fwd_bwd"] = tf(name, "fwd_bwd_tflops")
+    for name in ("fwd_fp8", "fwd_fp8_causal"):
+        if name in bd:
+            out[name] = pair(bd[name]["tflops"], bd[name]["frac_of_fp8_peak"])
+    if "gemm_peaks" in bd:
+        out["fp8_peak"] = bd["gemm_peaks"].get("fp8_peak_used")
+    for name in ("decode", "decode_paged"):
+        if name in bd:
+            out[name] = pair(bd[name]["gbps"], bd[name]["frac_of_hbm"])
+    return out
+
+
+def measure_gemm_peaks(dev, n=8192, reps=10):
+    """Dense GEMM rates on this GPU, timed the way the bf16 peak was: n^3 products, 2 n^3 FLOP,
+    best of ``reps`` CUDA-event timings after warm-up.  fp8 is torch._scaled_mm on e4m3 inputs
+    (unit scales, bf16 out); bf16 is torch.matmul, for the fp8 : bf16 ratio on the same box."""
+    import torch
+    out = {"n": n}
+
+    def best_ms(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(reps):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            fn()
+            e.record()
+            e.synchronize()
+            best = min(best, s.elapsed_time(e))
+        return best
+    flop = 2.0 * n ** 3
+    a = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    b = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    out["bf16_tflops_measured"] = round(flop / (best_ms(lambda: a @ b) * 1e-3) / 1e12, 1)
+    try:
+        a8 = a.to(torch.float8_e4m3fn)
+        b8 = b.to(torch.float8_e4m3fn).t()                # column-major second operand
+        one = torch.ones((), device=dev, dtype=torch.float32)
+        ms = best_ms(lambda: torch._scaled_mm(a8, b8, scale_a=one, scale_b=one, out_dtype=torch.bfloat16))
+        out["fp8_tflops_measured"] = round(flop / (ms * 1e-3) / 1e12, 1)
+    except (RuntimeError, AttributeError, TypeError) as ex:   # no fp8 GEMM in this torch build
+        out["fp8_error"] = str(ex).splitlines()[0][:120]
+    del a, b
+    return out
+
+
 # ---------------------------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------------------------
@@ -345,7 +420,7 @@ def run_ours(args, rank, world, local_rank):
         "kernel": "fa::bwd_main_kernel<128> (F3)",
         "work_per_launch": f"{fl_b:.4e} FLOP (10*d*N_q*N_kv*B*H)",
         "avg_launch_ms": round(bwd_main_ms, 4),
-        "peak_source": f"bf16_tflops (burst) of {peak_src} MEASURED_PEAKS.json",
+        "peak_source": f"bf16_tflops (burst), {peak_src}",
     }
 
     # ---- forward alone (F1 timed alone: one kernel per call)
@@ -420,8 +495,8 @@ def run_ours(args, rank, world, local_rank):
             "fwd_tflops": round(whole_job_rate(flx_f, world, mf * 1e-3) / 1e12, 1), "fwd_ms": round(mf, 4),
             "fwd_bwd_tflops": round(whole_job_rate(flx_f + flx_b, world, mfb * 1e-3) / 1e12, 1),
             "fwd_bwd_ms": round(mfb, 4),
-            "l2": "256 MB buffer written before every timed call (inputs fit in L2); per-call events"
-                  if small else "inputs exceed the 129 MB L2; per-call events",
+            "fwd_frac": round(flx_f / (mf * 1e-3) / 1e12 / peak_tf, 4),
+            "fwd_bwd_frac": round((flx_f + flx_b) / (mfb * 1e-3) / 1e12 / peak_tf, 4),
         }
         del xx, ox, lx, gx, wsx
     del l2_flush
@@ -448,11 +523,9 @@ def run_ours(args, rank, world, local_rank):
     ws_total, _ = timed(win_step, K)
     wf_ms, ws_ms = reduce_max(wf_total / K), reduce_max(ws_total / K)
     breakdown["window"] = {
-        "workload": f"{wl_.name} under a causal sliding window of {win + 1} keys (left {win}, right 0)",
         "fwd_tflops": round(whole_job_rate(fl_wf, world, wf_ms * 1e-3) / 1e12, 1), "fwd_ms": round(wf_ms, 4),
         "fwd_bwd_tflops": round(whole_job_rate(fl_wf + fl_wb, world, ws_ms * 1e-3) / 1e12, 1),
         "fwd_bwd_ms": round(ws_ms, 4),
-        "flops": "4 d (fwd) and 10 d (bwd) per visible (query, key) pair",
     }
     # ---- block-sparse on the same long sequence: 128 x 128 blocks, a band of one block either
     # side of the diagonal, the first key block and 5% random blocks, causal inside the blocks
@@ -472,12 +545,10 @@ def run_ours(args, rank, world, local_rank):
     bb_total, _ = timed(bs_step, K)
     bf_ms, bb_ms = reduce_max(bf_total / K), reduce_max(bb_total / K)
     breakdown["block_sparse"] = {
-        "workload": f"{wl_.name} under a causal block-sparse pattern (128x128 blocks: band of 1, first "
-                    f"key block, 5% random; {float(bmask.float().mean()):.3f} of blocks set)",
+        "density": round(float(bmask.float().mean()), 4),
         "fwd_tflops": round(whole_job_rate(fl_bf, world, bf_ms * 1e-3) / 1e12, 1), "fwd_ms": round(bf_ms, 4),
         "fwd_bwd_tflops": round(whole_job_rate(fl_bf + fl_bb, world, bb_ms * 1e-3) / 1e12, 1),
         "fwd_bwd_ms": round(bb_ms, 4),
-        "flops": "4 d (fwd) and 10 d (bwd) per visible (query, key) pair",
     }
     del xw, ow, lw, gw, wsw, bmask_d
 
@@ -507,18 +578,20 @@ def run_ours(args, rank, world, local_rank):
     vb_total, _ = timed(vl_step, K)
     vf_ms, vb_ms = reduce_max(vf_total / K), reduce_max(vb_total / K)
     breakdown["varlen"] = {
-        "workload": f"16 packed causal sequences of 512..8192 tokens (seed 1006: {vtot} tokens in all), "
-                    f"H={vH}, d={vd}",
+        "tokens": vtot,
         "fwd_tflops": round(whole_job_rate(fl_vf, world, vf_ms * 1e-3) / 1e12, 1), "fwd_ms": round(vf_ms, 4),
         "fwd_bwd_tflops": round(whole_job_rate(fl_vf + fl_vb, world, vb_ms * 1e-3) / 1e12, 1),
         "fwd_bwd_ms": round(vb_ms, 4),
-        "flops": "4 d (fwd) and 10 d (bwd) per visible (query, key) pair of each sequence",
     }
     del xv, ov, lv, gv, wsv
 
     # ---- FP8 forward (e4m3 Q, K, V with per-tensor scales) on the same shapes
     x8 = inputs.make_qkv_fp8(w.B, w.H, w.N_q, w.N_kv, w.d, w.seed + 7919 * rank, device=str(dev))
-    peak_f8 = 2 * peak_tf                    # nominal fp8 : bf16 dense ratio of 2 on this part
+    gemm = measure_gemm_peaks(dev)
+    if gemm.get("fp8_tflops_measured"):
+        peak_f8, peak_f8_src = gemm["fp8_tflops_measured"], "measured e4m3 GEMM, this run"
+    else:
+        peak_f8, peak_f8_src = 2 * peak_tf, "2 x bf16_tflops (nominal ratio; fp8 GEMM unavailable)"
 
     def fwd8(causal):
         def f(pe):
@@ -536,12 +609,11 @@ def run_ours(args, rank, world, local_rank):
         breakdown[key] = {"tflops": round(whole_job_rate(fl, world, ms8 * 1e-3) / 1e12, 1),
                           "ms": round(ms8, 4), "kernel_ms": round(k8, 4),
                           "frac_of_fp8_peak": round(fl / (k8 * 1e-3) / 1e12 / peak_f8, 4),
-                          "fp8_peak": peak_f8,
-                          "peak_source": "2 x bf16_tflops (burst, measured): nominal fp8/bf16 ratio",
                           "traffic": profiled_traffic("fwd_kernel<128, fp8>", source_digest(
                               "exact_io_aware_08_gb300/csrc/fwd.cu", "exact_io_aware_08_gb300/csrc/sm103.cuh"))
                           if not causal else None}
     del x8
+    breakdown["gemm_peaks"] = dict(gemm, fp8_peak_used=round(peak_f8, 1), fp8_peak_source=peak_f8_src)
 
     # ---- e2e through the public API with pinned host buffers (restore the headline inputs)
     host = {k_: x[k_].pin_memory() for k_ in ("q", "k", "v", "do")}
@@ -621,8 +693,7 @@ def run_ours(args, rank, world, local_rank):
     e_ms = reduce_max(es.elapsed_time(ee) / K)
     e2e = {"value": round(whole_job_rate(fl_f + fl_b, world, e_ms * 1e-3) / 1e12, 1), "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 4),
-           "api": "exact_io_aware_08_gb300.fa_fwd / fa_bwd (C ABI), pinned host buffers, copies on two "
-                  "streams overlapped with the neighbouring steps' compute (3 device buffer sets)"}
+           "api": "fa_fwd + fa_bwd (C ABI), pinned host buffers, 3 device buffer sets"}
     del dbuf, dout
     del d, x, host, out_host
     torch.cuda.empty_cache()
@@ -647,15 +718,14 @@ def run_ours(args, rank, world, local_rank):
     part = W.decode_partial_bytes(wd.B, wd.H, wd.d, wd.n_splits)
     gbs = bytes_dec / (statistics.mean(dk_inner) * 1e-3) / 1e9
     breakdown["decode"] = {
-        "workload": wd.name, "gbps": round(whole_job_rate(bytes_dec, world, dec_ms * 1e-3) / 1e9, 1),
+        "gbps": round(whole_job_rate(bytes_dec, world, dec_ms * 1e-3) / 1e9, 1),
         "ms": round(dec_ms, 4), "frac_of_hbm": round(gbs / peak_hbm, 4),
         "gbps_incl_partials": round((bytes_dec + part) / (statistics.mean(dk_inner) * 1e-3) / 1e9, 1),
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak_hbm, "unit": "GB/s",
                      "frac": round(gbs / peak_hbm, 4),
                      "traffic": profiled_traffic("decode_split_kernel<128>", source_digest(
                          "exact_io_aware_08_gb300/csrc/decode.cu", "exact_io_aware_08_gb300/csrc/sm103.cuh")),
-                     "kernels": "decode_split_kernel<128> + decode_merge_kernel<128> (one call)",
-                     "work_per_launch": f"{bytes_dec} B (K + V + q + O + lse)"},
+                     "work_per_launch": bytes_dec},
     }
 
     # ---- the same decode over a paged cache: 256-key blocks in a shuffled pool
@@ -686,10 +756,8 @@ def run_ours(args, rank, world, local_rank):
     dp_ms = reduce_max(dp_total / K)
     gbs_p = bytes_dec / (statistics.mean(dp_inner) * 1e-3) / 1e9
     breakdown["decode_paged"] = {
-        "workload": f"{wd.name}, paged cache (block_size {bs}, blocks shuffled over the pool)",
         "gbps": round(whole_job_rate(bytes_dec, world, dp_ms * 1e-3) / 1e9, 1),
         "ms": round(dp_ms, 4), "frac_of_hbm": round(gbs_p / peak_hbm, 4),
-        "kernels": "decode_split_kernel<128, paged> + decode_merge_kernel<128> (one call)",
         "traffic": profiled_traffic("decode_split_kernel<128, paged>", source_digest(
             "exact_io_aware_08_gb300/csrc/decode.cu", "exact_io_aware_08_gb300/csrc/sm103.cuh")),
     }
@@ -704,7 +772,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": f"{w.name} forward+backward, non-causal (headline)", "B": w.B, "H": w.H,
                    "N": w.N_q, "d": w.d, "causal": False, "scale": "1/sqrt(d)",
                    "step": "fa_fwd + fa_bwd_prep + fa_bwd_main + fa_bwd_finish",
-                   "l2": "no flush between steps: each step's inputs (Q, K, V, dO: 537 MB) exceed the 129 MB L2",
+                   "l2": "no flush: each step's inputs (537 MB) exceed the 129 MB L2",
                    "parallelism": f"dp{world} (independent batches per GPU)"},
         "frac_of_peak": round(value / world / peak_tf, 4),
         "breakdown": breakdown,
@@ -715,6 +783,8 @@ def run_ours(args, rank, world, local_rank):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         result["cpu_baseline"] = time_oracle(w)
+    # last key, so that a reader of the line's tail sees every workload's headline numbers
+    result["summary"] = summarize(breakdown, peak_tf)
     return result
 
 

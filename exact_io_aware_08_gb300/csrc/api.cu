@@ -61,6 +61,14 @@ fa_status_t check_shape(int B, int H, int n_q, int n_kv, int d, float scale) {
   return FA_OK;
 }
 
+// The decode kernels index their (b, h, chunk) work items with 32-bit ints.
+fa_status_t check_decode_items(int B, int H, int n_splits) {
+  const long long items = static_cast<long long>(B) * H * n_splits;
+  if (items >= (1LL << 31))
+    return fail(FA_ERR_UNSUPPORTED, "B*H*n_splits=%lld too large (limit 2^31 - 1)", items);
+  return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -405,6 +413,7 @@ size_t fa_decode_workspace_size(int B, int H, int N_kv, int d, int n_splits) {
   if (B < 1 || H < 1 || N_kv < 0 || (d != 64 && d != 128)) return 0;
   if (n_splits <= 0) n_splits = fa::decode_auto_splits(B, H, N_kv);
   if (n_splits > fa::kDecodeMaxSplits) return 0;
+  if (static_cast<long long>(B) * H * n_splits >= (1LL << 31)) return 0;
   return fa::decode_part_bytes(B, H, d, n_splits);
 }
 
@@ -417,6 +426,7 @@ fa_status_t fa_decode_splitkv(const fa_bf16_t* q, const fa_bf16_t* k, const fa_b
   if (n_splits > fa::kDecodeMaxSplits)
     return fail(FA_ERR_UNSUPPORTED, "n_splits=%d exceeds %d", n_splits, fa::kDecodeMaxSplits);
   if (n_splits <= 0) n_splits = fa::decode_auto_splits(B, H, N_kv);
+  if ((st = check_decode_items(B, H, n_splits)) != FA_OK) return st;
   if (!q || !o || !lse || (N_kv > 0 && (!k || !v)))
     return fail(FA_ERR_INVALID_ARG, "null pointer argument");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
@@ -443,6 +453,7 @@ fa_status_t fa_decode_splitkv_noalloc(const fa_bf16_t* q, const fa_bf16_t* k, co
   if (n_splits > fa::kDecodeMaxSplits)
     return fail(FA_ERR_UNSUPPORTED, "n_splits=%d exceeds %d", n_splits, fa::kDecodeMaxSplits);
   if (n_splits <= 0) n_splits = fa::decode_auto_splits(B, H, N_kv);
+  if ((st = check_decode_items(B, H, n_splits)) != FA_OK) return st;
   if (!q || !o || !lse || (N_kv > 0 && (!k || !v)))
     return fail(FA_ERR_INVALID_ARG, "null pointer argument");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
@@ -488,6 +499,7 @@ fa_status_t fa_decode_paged(const fa_bf16_t* q, const fa_bf16_t* k_cache,
   if (n_splits > fa::kDecodeMaxSplits)
     return fail(FA_ERR_UNSUPPORTED, "n_splits=%d exceeds %d", n_splits, fa::kDecodeMaxSplits);
   if (n_splits <= 0) n_splits = fa::decode_auto_splits(B, H, max_seqlen_k);
+  if ((st = check_decode_items(B, H, n_splits)) != FA_OK) return st;
   if (!q || !k_cache || !v_cache || !o || !lse || !block_table || !seqlens_k)
     return fail(FA_ERR_INVALID_ARG, "null pointer argument");
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||

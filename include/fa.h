@@ -158,7 +158,11 @@ fa_status_t fa_fwd_varlen(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_
 
 /*
  * Workspace bytes fa_bwd needs: an fp32 dQ accumulator [B,H,N_q,d] plus fp32 D [B,H,N_q]
- * plus alignment padding.  Returns 0 for unsupported arguments.
+ * plus alignment padding.  Returns 0 for unsupported arguments.  Both arrays come from
+ * [Lesson4] section 3 "Backward pass: recompute instead of store": step 3 forms
+ * D_i = dO_i . O_i once per query row, and step 4's dQ_i += scale dS K_j adds one term per key
+ * tile, which this library sums in fp32 across the CTAs of different key tiles.  N_kv does not
+ * change the size; it is taken so the signature matches fa_bwd's.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N_q, int N_kv, int d);
 
@@ -221,7 +225,11 @@ fa_status_t fa_bwd_varlen(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_
 
 /*
  * Workspace bytes fa_decode_splitkv needs for n_splits partial states per (b, h):
- * fp32 (m, l, o~[d]).  n_splits <= 0 means "automatic" (as fa_decode_splitkv chooses).
+ * fp32 (m, l, o~[d]), the per-chunk state of [Lesson4] section 3 "Split-KV for decoding
+ * (flash-decoding)" that the merge step combines.  n_splits <= 0 means "automatic" (as
+ * fa_decode_splitkv chooses).  The call takes N_kv because the automatic split count depends on
+ * it (at least ~256 keys per chunk); with an explicit n_splits N_kv does not change the size.
+ * Returns 0 for unsupported arguments (including B*H*n_splits >= 2^31).
  */
 size_t fa_decode_workspace_size(int B, int H, int N_kv, int d, int n_splits);
 
@@ -236,8 +244,8 @@ size_t fa_decode_workspace_size(int B, int H, int N_kv, int d, int n_splits);
  * ([Lesson4] section 3 "Merging two partial results"; empty chunks weigh 0).
  *
  * q: [B,H,1,d]; k, v: [B,H,N_kv,d]; o: [B,H,1,d]; lse: [B,H,1].  n_splits in [1, 1024], or
- * <= 0 for automatic.  ``ws`` holds at least fa_decode_workspace_size(...) bytes, 16-byte
- * aligned; contents on entry ignored.
+ * <= 0 for automatic; B*H*n_splits < 2^31 (else FA_ERR_UNSUPPORTED).  ``ws`` holds at least
+ * fa_decode_workspace_size(...) bytes, 16-byte aligned; contents on entry ignored.
  */
 fa_status_t fa_decode_splitkv(const fa_bf16_t* q, const fa_bf16_t* k, const fa_bf16_t* v,
                               fa_bf16_t* o, float* lse, int B, int H, int N_kv, int d,
@@ -292,6 +300,9 @@ fa_status_t fa_decode_paged(const fa_bf16_t* q, const fa_bf16_t* k_cache,
  *    FA_ERR_UNSUPPORTED before anything is launched.
  *  - The first call on a device looks up the scratch's device address (cudaGetSymbolAddress)
  *    with that device current; make that first call before any stream capture.
+ *    The address stays cached for the life of the process: after cudaDeviceReset the
+ *    library's device image may be reloaded elsewhere, so do not use this entry point after
+ *    resetting a device in the same process.
  *  - Every call shares the one array and leaves its contents behind.  Nothing in it needs to
  *    start at zero (each call writes every state it reads), but two calls whose kernels overlap
  *    on the GPU (different streams, or different host threads) race on it: serialise them.
@@ -303,9 +314,12 @@ fa_status_t fa_decode_splitkv_noalloc(const fa_bf16_t* q, const fa_bf16_t* k, co
 
 /*
  * fa_sync_status -- synchronise ``stream`` and report device-side failures recorded by any
- * kernel of this library since the last call (currently: a bounded pipeline wait that ran
- * out, FA_ERR_DEVICE_TIMEOUT).  Clears the recorded state.  Also returns FA_ERR_CUDA if the
- * stream reports an asynchronous CUDA error.
+ * kernel of this library since the last call (a bounded pipeline wait that ran out,
+ * FA_ERR_DEVICE_TIMEOUT; a bad varlen boundary or paged-cache entry, FA_ERR_INVALID_ARG).
+ * Clears the recorded state.  Also returns FA_ERR_CUDA if the stream reports an asynchronous
+ * CUDA error.  This is how the library fails loudly rather than handing back wrong results
+ * ([Scratch] "How this shows up in practice": a kernel that cannot do the job must say so,
+ * never fall back silently); the pages define no such call, only the behaviour.
  */
 fa_status_t fa_sync_status(void* stream);
 
@@ -335,7 +349,11 @@ fa_status_t fa_selftest_wait_timeout(unsigned int limit_us, void* stream);
  */
 fa_status_t fa_debug_counters(unsigned long long* device_counters);
 
-/* Static, human-readable name of a status code. */
+/*
+ * Static, human-readable name of a status code.  The pages have no counterpart; like
+ * fa_last_error_message it serves the loud failure [Scratch] "How this shows up in practice"
+ * asks for (an error the caller can print, not a silent fallback).
+ */
 const char* fa_status_string(fa_status_t status);
 
 /* One-line description of the last non-OK status returned on the calling thread. */

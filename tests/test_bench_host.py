@@ -85,3 +85,26 @@ def test_reference_arm_other_ranks_exit_without_work():
                         "--steps", "1", "--warmup", "3"], capture_output=True, text=True, timeout=120,
                        cwd=ROOT, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_summary_pairs_every_workload_with_its_fraction_of_peak():
+    import bench
+    bd = {
+        "fwd": {"tflops": 1400.0, "frac_of_peak": 0.72},
+        "fwd_bwd": {"tflops": 1100.0}, "fwd_causal": {"tflops": 1240.0}, "fwd_bwd_causal": {"tflops": 980.0},
+        "gpt2m_8x16x1024x64_causal": {"fwd_tflops": 350.0, "fwd_frac": 0.18, "fwd_bwd_tflops": 330.0,
+                                      "fwd_bwd_frac": 0.17},
+        "block_sparse": {"fwd_bwd_tflops": 520.0},
+        "fwd_fp8": {"tflops": 1950.0, "frac_of_fp8_peak": 0.6},
+        "gemm_peaks": {"fp8_peak_used": 3250.0},
+        "decode": {"gbps": 6950.0, "frac_of_hbm": 1.02},
+    }
+    s = bench.summarize(bd, 2000.0)
+    assert s["fwd"] == [1400.0, 0.72]
+    assert s["fwd_bwd"] == [1100.0, 0.55] and s["fwd_bwd_causal"] == [980.0, 0.49]
+    assert s["gpt2m_fwd"] == [350.0, 0.18] and s["gpt2m_fwd_bwd"] == [330.0, 0.17]
+    assert s["block_sparse_fwd_bwd"] == [520.0, 0.26]
+    assert s["fwd_fp8"] == [1950.0, 0.6] and s["fp8_peak"] == 3250.0
+    assert s["decode"] == [6950.0, 1.02]
+    assert "long_fwd" not in s and "varlen_fwd_bwd" not in s
+    assert len(json.dumps(s)) < 1000
