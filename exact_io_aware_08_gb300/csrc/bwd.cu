@@ -11,8 +11,8 @@
 //
 //   F2  bwd_pre:   D = rowsum(dO o O) in fp32; zero the fp32 dQ accumulator.
 //   F3  bwd_main:  one CTA per (128-key tile, head); 480 threads:
-//         warp 0     TMA producer: K_j, V_j once; Q_i, dO_i (+ lse_i, D_i) per query tile
-//                    through a 3-deep ring.
+//         warp 0     TMA producer: K_j, V_j once; Q_i, dO_i per query tile through a 3-deep
+//                    ring.  (lse_i and D_i are loaded by the dS warps themselves.)
 //         warp 1     TMEM owner and MMA issuer: S^T = K Q^T, dP^T = V dO^T (keys on TMEM
 //                    lanes), dV += P^T dO (P^T read from TMEM), dK += dS^T Q, and the dQ tile
 //                    product, issued per step as dV_i, S/dP_{i+1}, dK_i, dQ_i.
@@ -66,10 +66,7 @@ struct BwdCfg {
   // d = 128: staging of one fp32 dQ tile [BM queries][d] for the TMA reduce-add into dQ_acc
   static constexpr int DQS_BYTES = (D == 128) ? BM * D * 4 : 0;
   static constexpr int OFF_DQS = OFF_DS + 2 * DS_TILE;      // dS^T double-buffered
-  // per stage: -lse log2e [BM], -D [BM] (fp32), written by the producer warp
-  static constexpr int OFF_LSE = OFF_DQS + DQS_BYTES;
-  static constexpr int LSE_STAGE = 2 * BM * 4;
-  static constexpr int OFF_BAR = OFF_LSE + NST * LSE_STAGE;
+  static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
   // kv_full, stage_full[NST], stage_empty[NST], st_full, dp_full, p_ready, ds_ready,
   // pds_free[2], dq_full[2], dq_free[2], mma_done, dqs_sync, dqs_done[2]
   static constexpr int NBAR = 1 + 2 * NST + 14;
@@ -240,7 +237,7 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
     for (int s = 0; s < C::NST; ++s) {
-      mbar_init(&stage_full[s], 2);      // TMA bytes + the producer warp's lse/D writes
+      mbar_init(&stage_full[s], 1);      // TMA bytes
       mbar_init(&stage_empty[s], 1);
     }
     // st_full: the MMA's commit + the helper, which folds in "stage i loaded" (lse, D) and
@@ -301,16 +298,6 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
                         y2(q_beg, q0));
           }
         }
-        float* s_lse = reinterpret_cast<float*>(smem + C::OFF_LSE + s * C::LSE_STAGE);
-        float* s_del = s_lse + C::BM;
-        for (int e = lane; e < C::BM; e += 32) {
-          const int q = q0 + e;
-          const size_t li = VL ? static_cast<size_t>(head) * p.total_q + q_beg + q : qrow(q);
-          s_lse[e] = (q < n_q) ? -p.lse[li] * 1.4426950408889634f : -INFINITY;
-          s_del[e] = (q < n_q) ? -p.delta[qrow(q)] : 0.f;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&stage_full[s]);
         issued = i + 1;
       }
       if (!ok && lane == 0) {
@@ -414,26 +401,25 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
     const bool row_dead = k_idx >= n_kv;
     const float c2 = p.scale_log2;
     bool ok = true;
+    // -lse (log2 units) and -D of query column q of the step: lane l loads column l from global
+    // memory (L1/L2 hits: every dS warp of a group reads the same columns) and shuffles pass the
+    // values round.  The loads are issued before the wait for S_i, which hides their latency.
+    auto nlse_of = [&](int q) -> float {
+      const size_t li = VL ? static_cast<size_t>(head) * p.total_q + q_beg + q : qrow(q);
+      return (q < n_q) ? -__ldg(p.lse + li) * 1.4426950408889634f : -INFINITY;
+    };
+    auto nd_of = [&](int q) -> float { return (q < n_q) ? -__ldg(p.delta + qrow(q)) : 0.f; };
     for (int i = 0; i < n; ++i) {
       const int q0 = step_q0(i);
-      // -lse (log2 units) and -D of the step's columns, the same for every thread: lane l reads
-      // column l once and shuffles pass the values round (a uniform-address shared load costs a
-      // shared-memory wavefront per 4 bytes delivered).  The first 32 columns are fetched while
-      // the warps would otherwise wait for S_i: stage i is waited for directly here.
-      if (!(ok = mbar_wait_warp(&stage_full[i % C::NST], (i / C::NST) & 1, abort_flag, 225))) break;
-      const float* s_nlse = reinterpret_cast<const float*>(smem + C::OFF_LSE + (i % C::NST) * C::LSE_STAGE);
-      const float* s_nd = s_nlse + C::BM;
       float lane_nd[C::HALF / 32], nl0[32];
-      {
-        const float lane_nl = s_nlse[cb + lane];
-        lane_nd[0] = s_nd[cb + lane];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) nl0[e] = __shfl_sync(0xffffffffu, lane_nl, e);
-      }
-      // st_full(i): S_i is done, stage i (lse, D) is loaded and dS^T buffer i & 1 is free
-      // (the last two folded in by the helper); dp_full(i), waited for below: dP_i is done
+      const float lane_nl = nlse_of(q0 + cb + lane);
+      lane_nd[0] = nd_of(q0 + cb + lane);
+      // st_full(i): S_i is done, stage i is loaded and dS^T buffer i & 1 is free (the last two
+      // folded in by the helper); dp_full(i), waited for below: dP_i is done
       if (!(ok = mbar_wait_warp(st_full, i & 1, abort_flag, 221))) break;
       tc_fence_after();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) nl0[e] = __shfl_sync(0xffffffffu, lane_nl, e);
       // a (key tile, query tile) pair that some pair of rows sees only in part
       const bool diag = WIN ? ((q0 < k0 + C::BN - 1 - wr) || (q0 + C::BM - 1 > k0 + wl))
                             : (p.causal && (q0 < k0 + C::BN - 1));
@@ -462,10 +448,10 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) nl[e] = nl0[e];
         } else {
-          const float lane_nl = s_nlse[cb + c * 32 + lane];
-          lane_nd[c] = s_nd[cb + c * 32 + lane];
+          const float lane_nl_c = nlse_of(q0 + cb + c * 32 + lane);
+          lane_nd[c] = nd_of(q0 + cb + c * 32 + lane);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) nl[e] = __shfl_sync(0xffffffffu, lane_nl, e);
+          for (int e = 0; e < 32; ++e) nl[e] = __shfl_sync(0xffffffffu, lane_nl_c, e);
         }
         tmem_wait_ld();
         uint32_t pk_p[16];
@@ -717,13 +703,17 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
 // the per-CTA start (barriers, TMEM, first loads) and the dK/dV epilogue from every item but
 // the CTA's first and last, which is most of a short key tile's time.
 // ------------------------------------------------------------------------------------------
-// Key tiles per head up to which the persistent backward runs (d = 64).  Measured on GB300:
-// at 4 key tiles (512 tokens) it is 10% faster than one CTA per key tile; at 8 (a GPT-2-medium
-// layer) 2% slower and at 16 up to 15% slower: its steps run slower than bwd_main_kernel's
-// (also when launched with one CTA per item), which outweighs the per-CTA start and epilogue
-// it saves once items are longer than a few steps.
+// Key tiles per head up to which the persistent backward runs (d = 64).  Measured on GB300 with
+// the L2 flushed before each call: at 4 key tiles (512 tokens) it is 8-10% faster than one CTA
+// per key tile; at 8 it wins for causal heads (a GPT-2-medium layer, whose causal key tiles
+// average 4.5 steps: 0.136 -> 0.130 ms) and loses 2% for unmasked ones; at 16 it is up to 15%
+// slower: its steps run slower than bwd_main_kernel's (also when launched with one CTA per
+// item), which outweighs the per-CTA start and epilogue it saves once items are longer than a
+// few steps.
 constexpr int kPersistentBwdMaxKvTiles = 4;
-inline bool use_persistent_bwd(int n_kvtiles) { return n_kvtiles <= kPersistentBwdMaxKvTiles; }
+inline bool use_persistent_bwd(int n_kvtiles, bool causal) {
+  return n_kvtiles <= (causal ? 2 * kPersistentBwdMaxKvTiles : kPersistentBwdMaxKvTiles);
+}
 
 struct BwdP64 {
   using B = BwdCfg<64>;
@@ -732,8 +722,7 @@ struct BwdP64 {
   static constexpr int OFF_V = 2 * B::KV_TILE;
   static constexpr int OFF_ST = 3 * B::KV_TILE;         // Q, dO ring
   static constexpr int OFF_DS = OFF_ST + NST * B::STAGE;
-  static constexpr int OFF_LSE = OFF_DS + 2 * B::DS_TILE;
-  static constexpr int OFF_BAR = OFF_LSE + NST * B::LSE_STAGE;
+  static constexpr int OFF_BAR = OFF_DS + 2 * B::DS_TILE;
   // k_full[2], k_free[2], v_full, v_free, stage_full[NST], stage_empty[NST], st_full, dp_full,
   // p_ready, ds_ready, dq_full[2], dq_free[2], acc_full, acc_free, mma_done, dqs_sync,
   // dqs_done[2]
@@ -817,7 +806,7 @@ bwd_persistent_kernel64(const __grid_constant__ BwdParams p) {
     mbar_init(v_full, 1);
     mbar_init(v_free, 1);
     for (int s = 0; s < C::NST; ++s) {
-      mbar_init(&stage_full[s], 2);
+      mbar_init(&stage_full[s], 1);      // TMA bytes
       mbar_init(&stage_empty[s], 1);
     }
     mbar_init(st_full, 2);
@@ -872,16 +861,6 @@ bwd_persistent_kernel64(const __grid_constant__ BwdParams p) {
           tma_load_3d(st, &p.tq, &stage_full[s], 0, q0, it.bh);
           tma_load_3d(st + B::Q_TILE, &p.tdo, &stage_full[s], 0, q0, it.bh);
         }
-        float* s_lse = reinterpret_cast<float*>(smem + C::OFF_LSE + s * B::LSE_STAGE);
-        float* s_del = s_lse + C::BM;
-        for (int e = lane; e < C::BM; e += 32) {
-          const int q = q0 + e;
-          const size_t li = static_cast<size_t>(it.bh) * p.n_q + q;
-          s_lse[e] = (q < p.n_q) ? -p.lse[li] * 1.4426950408889634f : -INFINITY;
-          s_del[e] = (q < p.n_q) ? -p.delta[li] : 0.f;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&stage_full[s]);
         issued = g + 1;
         if (i == 0) {
           // V of item j, once item j - 1's last dP product is done with the buffer
@@ -1021,18 +1000,22 @@ bwd_persistent_kernel64(const __grid_constant__ BwdParams p) {
       const bool row_dead = k_idx >= p.n_kv;
       for (int i = 0; i < it.n; ++i, ++g) {
         const int q0 = (it.i_start + i) * C::BM;
-        if (!(ok = mbar_wait_warp(&stage_full[g % C::NST], (g / C::NST) & 1, abort_flag, 325))) break;
-        const float* s_nlse = reinterpret_cast<const float*>(smem + C::OFF_LSE + (g % C::NST) * B::LSE_STAGE);
-        const float* s_nd = s_nlse + C::BM;
+        // -lse (log2 units) and -D of the step's query columns, loaded from global memory before
+        // the wait for S (see bwd_main_kernel)
+        auto nlse_of = [&](int q) -> float {
+          return (q < p.n_q) ? -__ldg(p.lse + static_cast<size_t>(it.bh) * p.n_q + q) * 1.4426950408889634f
+                             : -INFINITY;
+        };
+        auto nd_of = [&](int q) -> float {
+          return (q < p.n_q) ? -__ldg(p.delta + static_cast<size_t>(it.bh) * p.n_q + q) : 0.f;
+        };
         float lane_nd[C::HALF / 32], nl0[32];
-        {
-          const float lane_nl = s_nlse[cb + lane];
-          lane_nd[0] = s_nd[cb + lane];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) nl0[e] = __shfl_sync(0xffffffffu, lane_nl, e);
-        }
+        const float lane_nl = nlse_of(q0 + cb + lane);
+        lane_nd[0] = nd_of(q0 + cb + lane);
         if (!(ok = mbar_wait_warp(st_full, g & 1, abort_flag, 321))) break;
         tc_fence_after();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) nl0[e] = __shfl_sync(0xffffffffu, lane_nl, e);
         const bool diag = p.causal && (q0 < k0 + C::BN - 1);
         uint32_t pk_ds[C::HALF / 2];
         uint32_t ppk[C::HALF / 2];                   // P as bf16 pairs (see bwd_main_kernel)
@@ -1046,10 +1029,10 @@ bwd_persistent_kernel64(const __grid_constant__ BwdParams p) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) nl[e] = nl0[e];
           } else {
-            const float lane_nl = s_nlse[cb + cc * 32 + lane];
-            lane_nd[cc] = s_nd[cb + cc * 32 + lane];
+            const float lane_nl_c = nlse_of(q0 + cb + cc * 32 + lane);
+            lane_nd[cc] = nd_of(q0 + cb + cc * 32 + lane);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) nl[e] = __shfl_sync(0xffffffffu, lane_nl, e);
+            for (int e = 0; e < 32; ++e) nl[e] = __shfl_sync(0xffffffffu, lane_nl_c, e);
           }
           tmem_wait_ld();
           uint32_t pk_p[16];
@@ -1339,7 +1322,7 @@ static cudaError_t launch_bwd_main_d(const BwdArgs& a, cudaStream_t stream) {
     return cudaGetLastError();
   }
   if constexpr (D == 64) {
-    if (!a.windowed && use_persistent_bwd(p.n_kvtiles)) {
+    if (!a.windowed && use_persistent_bwd(p.n_kvtiles, a.causal != 0)) {
       static int attr_p[64] = {0};
       cudaError_t e = ensure_smem_attr(bwd_persistent_kernel64, BwdP64::SMEM_BYTES, attr_p);
       if (e != cudaSuccess) return e;

@@ -203,12 +203,21 @@ cudaError_t decode_noalloc_scratch(float** ptr);
 
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (kernel, device).  ``done`` is a
 // per-kernel flag array owned by the caller (kernels of the same signature must not share one).
+// A kernel that moves registers between warpgroups with setmaxnreg passes its thread count and
+// the registers its split needs: setmaxnreg draws only on what the CTA was launched with
+// (threads x registers per thread, the compiler's choice), and a split above that would wait
+// forever, so the launch is refused (cudaErrorInvalidConfiguration) instead.
 template <typename F>
-cudaError_t ensure_smem_attr(F* func, int bytes, int (&done)[64]) {
+cudaError_t ensure_smem_attr(F* func, int bytes, int (&done)[64], int threads = 0, int reg_need = 0) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && __atomic_load_n(&done[dev], __ATOMIC_ACQUIRE)) return cudaSuccess;
+  if (reg_need > 0) {
+    cudaFuncAttributes at;
+    if ((e = cudaFuncGetAttributes(&at, func)) != cudaSuccess) return e;
+    if (at.numRegs * threads < reg_need) return cudaErrorInvalidConfiguration;
+  }
   e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess && dev < 64) __atomic_store_n(&done[dev], 1, __ATOMIC_RELEASE);
   return e;

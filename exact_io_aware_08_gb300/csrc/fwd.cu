@@ -100,6 +100,13 @@ struct FwdCfg {
   static constexpr uint32_t BAR_P_THREADS = 128 + 32 + 32;
 };
 
+// Registers the setmaxnreg split of a forward configuration needs: warpgroup 0 at REG_CTRL,
+// the two softmax warpgroups at REG_SOFTMAX.
+template <typename Cfg>
+constexpr int reg_split_need() {
+  return 128 * static_cast<int>(Cfg::REG_CTRL) + 256 * static_cast<int>(Cfg::REG_SOFTMAX);
+}
+
 struct FwdParams {
   CUtensorMap tq, tk, tv, to;
   float* lse;
@@ -1236,7 +1243,7 @@ static cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   const uint64_t grid = static_cast<uint64_t>(p.n_qpairs) * bh;
   if (a.block_mask != nullptr) {
     static int attr_bs[64] = {0};
-    cudaError_t e = ensure_smem_attr(fwd_kernel<D, false, false, false, true>, C::SMEM_BYTES, attr_bs);
+    cudaError_t e = ensure_smem_attr(fwd_kernel<D, false, false, false, true>, C::SMEM_BYTES, attr_bs, C::THREADS, reg_split_need<C>());
     if (e != cudaSuccess) return e;
     log_launch("fwd_kernel<D, false, false, false, true>", static_cast<unsigned long long>(static_cast<unsigned>(grid)), C::THREADS, static_cast<unsigned long long>(C::SMEM_BYTES));
     fwd_kernel<D, false, false, false, true><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
@@ -1248,7 +1255,7 @@ static cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
     // one-CTA-per-item kernel runs its steps faster and wins)
     using PC = FwdPCfg<D>;
     static int attr_p[64] = {0};
-    cudaError_t e = ensure_smem_attr(fwd_persistent_kernel<D>, PC::SMEM_BYTES, attr_p);
+    cudaError_t e = ensure_smem_attr(fwd_persistent_kernel<D>, PC::SMEM_BYTES, attr_p, PC::THREADS, reg_split_need<PC>());
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
@@ -1261,13 +1268,13 @@ static cudaError_t launch_fwd_d(const FwdArgs& a, cudaStream_t stream) {
   }
   if (a.windowed) {
     static int attr_win[64] = {0};
-    cudaError_t e = ensure_smem_attr(fwd_kernel<D, false, false, true>, C::SMEM_BYTES, attr_win);
+    cudaError_t e = ensure_smem_attr(fwd_kernel<D, false, false, true>, C::SMEM_BYTES, attr_win, C::THREADS, reg_split_need<C>());
     if (e != cudaSuccess) return e;
     log_launch("fwd_kernel<D, false, false, true>", static_cast<unsigned long long>(static_cast<unsigned>(grid)), C::THREADS, static_cast<unsigned long long>(C::SMEM_BYTES));
     fwd_kernel<D, false, false, true><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
     return cudaGetLastError();
   }
-  cudaError_t e = ensure_smem_attr(fwd_kernel<D, false>, C::SMEM_BYTES, attr_done);
+  cudaError_t e = ensure_smem_attr(fwd_kernel<D, false>, C::SMEM_BYTES, attr_done, C::THREADS, reg_split_need<C>());
   if (e != cudaSuccess) return e;
   log_launch("fwd_kernel<D, false>", static_cast<unsigned long long>(static_cast<unsigned>(grid)), C::THREADS, static_cast<unsigned long long>(C::SMEM_BYTES));
   fwd_kernel<D, false><<<static_cast<unsigned>(grid), C::THREADS, C::SMEM_BYTES, stream>>>(p);
@@ -1306,7 +1313,7 @@ static cudaError_t launch_fwd_varlen_d(const FwdVarlenArgs& a, cudaStream_t stre
   p.block_mask = nullptr;
   p.bm_per_head = p.n_qblocks = 0;
   static int attr_done[64] = {0};
-  cudaError_t e = ensure_smem_attr(fwd_kernel<D, true>, C::SMEM_BYTES, attr_done);
+  cudaError_t e = ensure_smem_attr(fwd_kernel<D, true>, C::SMEM_BYTES, attr_done, C::THREADS, reg_split_need<C>());
   if (e != cudaSuccess) return e;
   const uint64_t grid = static_cast<uint64_t>(p.n_qpairs) * a.n_seqs * a.H;
   if (grid == 0) return cudaSuccess;
@@ -1346,7 +1353,7 @@ cudaError_t launch_fwd_fp8(const FwdArgs& a, cudaStream_t stream) {
   p.block_mask = nullptr;
   p.bm_per_head = p.n_qblocks = 0;
   static int attr_done[64] = {0};
-  cudaError_t e = ensure_smem_attr(fwd_kernel<D, false, true>, C::SMEM_BYTES, attr_done);
+  cudaError_t e = ensure_smem_attr(fwd_kernel<D, false, true>, C::SMEM_BYTES, attr_done, C::THREADS, reg_split_need<C>());
   if (e != cudaSuccess) return e;
   const uint64_t grid = static_cast<uint64_t>(p.n_qpairs) * bh;
   log_launch("fwd_kernel<D, false, true>", static_cast<unsigned long long>(static_cast<unsigned>(grid)), C::THREADS, static_cast<unsigned long long>(C::SMEM_BYTES));

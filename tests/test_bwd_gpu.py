@@ -118,13 +118,14 @@ def test_bwd_long_workload_with_outliers_sampled():
 
 
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("N", [300, 512])
+@pytest.mark.parametrize("N", [300, 512, 1000])
 def test_bwd_short_heads_many_items_per_cta(causal, N):
-    """Short heads at d = 64 (up to 4 key tiles) run on the persistent backward, each CTA taking
-    several (head, key tile) items (4 x 32 heads x 3 or 4 key tiles): dK and dV must agree bit
-    for bit with the one-CTA-per-tile kernel (which the windowed entry point runs for the same
-    mask), dQ (summed across key tiles in a run-dependent order) within the tolerance, and all
-    three with the oracle on sampled heads."""
+    """Short heads at d = 64 (up to 4 key tiles, or 8 with causal) run on the persistent
+    backward, each CTA taking several (head, key tile) items (4 x 32 heads x 3, 4 or 8 key
+    tiles): dK and dV must agree bit for bit with the one-CTA-per-tile kernel (which the windowed
+    entry point runs for the same mask), dQ (summed across key tiles in a run-dependent order)
+    within the tolerance, and all three with the oracle on sampled heads.  (1000 unmasked runs
+    the one-CTA-per-tile kernel on both sides.)"""
     require_gpu()
     B, H, d = 4, 32, 64
     scale = d ** -0.5
