@@ -827,7 +827,9 @@ struct FwdPCfg {
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   static constexpr uint32_t TMEM_COLS = 512, T_S = 0, T_O = 256;
   static constexpr int THREADS = 384;
-  static constexpr uint32_t REG_CTRL = 80, REG_SOFTMAX = 208;
+  // setmaxnreg split (launched with 168 per thread: 64512): 128 x 88 + 256 x 200 = 62464.  The
+  // item loop keeps more state live than fwd_kernel's; at 80 / 208 the control warps spilled.
+  static constexpr uint32_t REG_CTRL = 88, REG_SOFTMAX = 200;
   static constexpr float RESCALE_THRESHOLD = 8.f;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget (227 KB per CTA)");
 };
@@ -1111,18 +1113,18 @@ fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
           }
           if (j > 0) {                          // O_t settled: PV_t(j-1) preceded S_t(j)
 #pragma unroll
-            for (int kk = 0; kk < D / 32; ++kk) {
-              uint32_t rr[32];
-              tmem_ld32(t_o + kk * 32, rr);
+            for (int kk = 0; kk < D / 16; ++kk) {  // 16 columns at a time (s[] is live here)
+              uint32_t rr[16];
+              tmem_ld16(t_o + kk * 16, rr);
               tmem_wait_ld();
 #pragma unroll
-              for (int i = 0; i < 32; i += 2) {
+              for (int i = 0; i < 16; i += 2) {
                 const float2 v = fmul2(make_float2(__uint_as_float(rr[i]), __uint_as_float(rr[i + 1])),
                                        make_float2(alpha, alpha));
                 rr[i] = __float_as_uint(v.x);
                 rr[i + 1] = __float_as_uint(v.y);
               }
-              tmem_st32(t_o + kk * 32, rr);
+              tmem_st16(t_o + kk * 16, rr);
             }
           }
         }
