@@ -409,6 +409,9 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       return (q < n_q) ? -__ldg(p.lse + li) * 1.4426950408889634f : -INFINITY;
     };
     auto nd_of = [&](int q) -> float { return (q < n_q) ? -__ldg(p.delta + qrow(q)) : 0.f; };
+    // a warp none of whose key rows is past the keys' end (only a ragged last key tile has some)
+    bool warp_live = false;
+    if constexpr (D == 128) warp_live = !__any_sync(0xffffffffu, row_dead);
     for (int i = 0; i < n; ++i) {
       const int q0 = step_q0(i);
       float lane_nd[C::HALF / 32], nl0[32];
@@ -423,6 +426,9 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       // a (key tile, query tile) pair that some pair of rows sees only in part
       const bool diag = WIN ? ((q0 < k0 + C::BN - 1 - wr) || (q0 + C::BM - 1 > k0 + wl))
                             : (p.causal && (q0 < k0 + C::BN - 1));
+      // d = 128: nothing to mask in this step for this warp, so no per-element tests (measured:
+      // -1.2% unmasked, -1.6% causal at 4x32x4096; at d = 64 the same form was 13-15% slower)
+      const bool plain = D == 128 && !WIN && !diag && warp_live;
       const float2 c2v = make_float2(c2, c2);
       const int c_lo = k_idx - wr - q0, c_hi = k_idx + wl - q0;
       uint32_t pk_ds[C::HALF / 2];
@@ -461,13 +467,15 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
           const float2 x = ffma2(make_float2(__uint_as_float(rs[e]), __uint_as_float(rs[e + 1])), c2v,
                                  make_float2(nl[e], nl[e + 1]));
           float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
-          if constexpr (WIN) {
-            // query q0 + col sees key k_idx iff c_lo <= col <= c_hi
-            if (row_dead || (diag && (col < c_lo || col > c_hi))) p0 = 0.f;
-            if (row_dead || (diag && (col + 1 < c_lo || col + 1 > c_hi))) p1 = 0.f;
-          } else {
-            if (row_dead || (diag && k_idx > q0 + col)) p0 = 0.f;
-            if (row_dead || (diag && k_idx > q0 + col + 1)) p1 = 0.f;
+          if (!plain) {
+            if constexpr (WIN) {
+              // query q0 + col sees key k_idx iff c_lo <= col <= c_hi
+              if (row_dead || (diag && (col < c_lo || col > c_hi))) p0 = 0.f;
+              if (row_dead || (diag && (col + 1 < c_lo || col + 1 > c_hi))) p1 = 0.f;
+            } else {
+              if (row_dead || (diag && k_idx > q0 + col)) p0 = 0.f;
+              if (row_dead || (diag && k_idx > q0 + col + 1)) p1 = 0.f;
+            }
           }
           pk_p[e / 2] = pack_bf16x2(p0, p1);
           if constexpr (kPackedP) {
