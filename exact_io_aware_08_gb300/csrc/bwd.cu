@@ -95,7 +95,7 @@ struct BwdParams {
   float* dq_acc;
   int n_q, n_kv, n_qtiles, n_kvtiles, causal;
   float scale, scale_log2;
-  // Variable-length batches (packed token-major [total, H, d]; lse [H, total_q]; D and the dQ
+  // Variable-length batches (packed token-major [total, H, d]; lse and D [H, total_q]; the dQ
   // accumulator in the packed row order (token * H + head)).
   int heads, total_q, total_k, max_q, max_k;
   const int* cu_q;
@@ -408,7 +408,10 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       const size_t li = VL ? static_cast<size_t>(head) * p.total_q + q_beg + q : qrow(q);
       return (q < n_q) ? -__ldg(p.lse + li) * 1.4426950408889634f : -INFINITY;
     };
-    auto nd_of = [&](int q) -> float { return (q < n_q) ? -__ldg(p.delta + qrow(q)) : 0.f; };
+    auto nd_of = [&](int q) -> float {
+      const size_t di = VL ? static_cast<size_t>(head) * p.total_q + q_beg + q : qrow(q);
+      return (q < n_q) ? -__ldg(p.delta + di) : 0.f;
+    };
     // a warp none of whose key rows is past the keys' end (only a ragged last key tile has some)
     bool warp_live = false;
     if constexpr (D == 128) warp_live = !__any_sync(0xffffffffu, row_dead);
@@ -1225,7 +1228,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
                                                       const uint16_t* __restrict__ dO,
                                                       float* __restrict__ delta,
                                                       float4* __restrict__ dq_acc4,
-                                                      long long rows, long long acc4) {
+                                                      long long rows, long long acc4, int vl_heads) {
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long nthr = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long x = tid; x < acc4; x += nthr) dq_acc4[x] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1251,7 +1254,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
     }
 #pragma unroll
     for (int off = TPR / 2; off >= 1; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (valid && part == 0) delta[row] = s;
+    // packed variable-length rows (token * H + head) go head-major (head * total + token), the
+    // order in which the main kernel's dS warps read a query tile's D (as they read lse)
+    if (valid && part == 0) delta[vl_heads > 0 ? (row % vl_heads) * (rows / vl_heads) + row / vl_heads : row] = s;
   }
 }
 
@@ -1277,7 +1282,7 @@ static cudaError_t launch_bwd_prep_d(const BwdArgs& a, cudaStream_t stream) {
   log_launch("bwd_pre_kernel<D>", static_cast<unsigned long long>(std::max(blocks, 1)), 256, static_cast<unsigned long long>(0));
   bwd_pre_kernel<D><<<std::max(blocks, 1), 256, 0, stream>>>(
       static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dO), a.delta,
-      reinterpret_cast<float4*>(a.dq_acc), rows, acc4);
+      reinterpret_cast<float4*>(a.dq_acc), rows, acc4, a.cu_q != nullptr ? a.H : 0);
   return cudaGetLastError();
 }
 
