@@ -36,6 +36,10 @@ SHAPES = [
     (1, 1, 640, 640, 128, False),
     (3, 4, 700, 700, 128, True),     # 12 heads: causal items ordered across a full and a partial group
     (3, 3, 300, 300, 64, True),      # 9 heads, d = 64
+    # one-CTA-per-item kernel with an empty second query tile in the last item (its MMA thread
+    # has no work for more steps than the K/V ring is deep)
+    (1, 2, 2100, 2100, 128, True),
+    (1, 1, 4224, 4224, 64, False),
 ]
 
 
