@@ -44,6 +44,9 @@ CASES = [
     ([37, 200, 400], [90, 15, 700], 2, 128, False),          # different q and k lengths
     ([50, 0, 80], [60, 0, 80], 2, 64, False),                # an empty sequence
     ([40, 70], [0, 33], 1, 128, False),                      # a sequence with no keys
+    # long packed sequences, as in the bench's varlen workload: many tiles, ragged last pairs
+    ([3000, 17, 4100], None, 2, 128, True),
+    ([2500, 700], None, 2, 64, False),
 ]
 
 
@@ -97,6 +100,8 @@ BWD_CASES = [
     ([64, 257, 5, 1000], None, 3, 64, True),
     ([37, 200, 400], [90, 15, 700], 2, 128, False),
     ([50, 0, 80], [60, 0, 80], 2, 64, False),
+    ([3000, 17, 4100], None, 2, 128, True),
+    ([2500, 700], None, 2, 64, False),
 ]
 
 
