@@ -43,6 +43,10 @@ SHAPES = [
     (3, 4, 700, 700, 128, True),     # 12 heads: causal items ordered across a full and a partial group
     (3, 3, 300, 300, 64, True),      # 9 heads, d = 64
     (1, 2, 77, 1000, 64, False),
+    # longer heads on the one-CTA-per-key-tile kernels: 33 query steps with a ragged last one
+    # (d = 128, causal), 18 key tiles of 128-query steps (d = 64)
+    (1, 2, 2100, 2100, 128, True),
+    (1, 1, 2304, 2304, 64, False),
 ]
 
 
