@@ -33,6 +33,7 @@ FWD_CASES = [
     (1, 1, 640, 64, -1, 130),         # bounded on the right only
     (1, 2, 513, 128, 700, 3),         # window wider than the sequence on the left
     (1, 1, 256, 128, 127, 128),       # edges exactly on tile boundaries
+    (1, 2, 2500, 64, 600, 0),         # many key tiles per query tile at d = 64
 ]
 
 
@@ -72,6 +73,7 @@ BWD_CASES = [
     (1, 2, 700, 64, 50, 50),
     (2, 1, 777, 128, 5, 0),
     (1, 2, 600, 128, -1, 200),
+    (1, 2, 2500, 64, 600, 0),
 ]
 
 
