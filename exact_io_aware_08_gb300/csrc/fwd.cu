@@ -695,8 +695,7 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
           rs[k & 3] = fadd2(rs[k & 3], make_float2(p0, p1));
           // lb sums the bf16 weights the PV product uses, so O / lb is an exact weighted
           // average of V under those weights; lse keeps the fp32 sum
-          rb[k & 3] = fadd2(rb[k & 3], make_float2(__uint_as_float(pk[k] << 16),
-                                                   __uint_as_float(pk[k] & 0xffff0000u)));
+          rb[k & 3] = add_bf16x2_f32(rb[k & 3], pk[k]);
         }
         tmem_st32(t_s + h * 32, pk);
       }
@@ -1142,8 +1141,7 @@ fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
             pk[kk] = pack_bf16x2(p0, p1);
             rs[kk & 3] = fadd2(rs[kk & 3], make_float2(p0, p1));
             // lb sums the bf16 weights the PV product uses (O / lb is their exact average)
-            rb[kk & 3] = fadd2(rb[kk & 3], make_float2(__uint_as_float(pk[kk] << 16),
-                                                       __uint_as_float(pk[kk] & 0xffff0000u)));
+            rb[kk & 3] = add_bf16x2_f32(rb[kk & 3], pk[kk]);
           }
           tmem_st32(t_s + h * 32, pk);
         }

@@ -171,6 +171,16 @@ __device__ __forceinline__ bool warps_sync(uint64_t* bar, uint32_t parity,
   return mbar_wait_warp(bar, parity, abort_flag, where);
 }
 
+// acc.x += lo(pk), acc.y += hi(pk) for a pair of bf16 values packed in one word: the exact
+// bf16 -> fp32 widening is folded into a mixed-precision add (one instruction per element,
+// the same sums bit for bit as widening by shifts and masks first).
+__device__ __forceinline__ float2 add_bf16x2_f32(float2 acc, uint32_t pk) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y) : "r"(pk));
+  return acc;
+}
+
 // ------------------------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor)
 // ------------------------------------------------------------------------------------------
