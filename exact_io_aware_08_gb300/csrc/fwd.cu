@@ -67,7 +67,14 @@ struct FwdCfg {
   static constexpr int OFF_V = OFF_K + NS * TILE;
   // O staging: the dead Q tiles when they are as large as O tiles (bf16), else its own space
   static constexpr int OFF_OST = F8 ? OFF_V + NS * TILE : OFF_Q;
-  static constexpr int OFF_BAR = F8 ? OFF_OST + 2 * OTILE : OFF_V + NS * TILE;
+  // d = 64: O_t carries 16 more columns, which the PV product fills against a block of ones
+  // placed right after the V ring, so that they hold sum_j bf16(p_j), O's normaliser, formed
+  // on the tensor core (and rescaled with O) instead of by the softmax threads.  d = 128 has no
+  // TMEM left for them.
+  static constexpr bool LB_MMA = D == 64 && !F8;
+  static constexpr int DO = LB_MMA ? D + 16 : D;      // TMEM columns of O_t
+  static constexpr int OFF_ONES = OFF_V + NS * TILE;  // [128 keys x 64 columns], LB_MMA only
+  static constexpr int OFF_BAR = F8 ? OFF_OST + 2 * OTILE : OFF_ONES + (LB_MMA ? CHUNK : 0);
   // q_full, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[2], p_full[2], o_done[2]
   static constexpr int NBAR = 1 + 4 * NS + 6;
   // TMEM slot, abort flag, block-sparse stream length and live counts of the two query tiles
@@ -76,9 +83,11 @@ struct FwdCfg {
   static constexpr int OFF_BSL = OFF_MISC + 32;
   static constexpr int OFF_BSB = OFF_BSL + 2 * kBlockSparseMaxTiles;
   static constexpr int SMEM_BYTES = OFF_BSB + kBlockSparseMaxTiles + 1024;   // + 1 KB alignment slack
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget (227 KB per CTA)");
   static constexpr uint32_t TMEM_COLS = 512;
   static constexpr uint32_t T_S = 0;                  // S_t at columns [128 t, 128 t + 128)
-  static constexpr uint32_t T_O = 256;                // O_t at columns [256 + d t, ...)
+  static constexpr uint32_t T_O = 256;                // O_t at columns [256 + DO t, ...)
+  static_assert(T_O + 2 * DO <= TMEM_COLS, "TMEM budget");
   static constexpr int THREADS = 384;
   // setmaxnreg split: launched with 168 per thread (384 x 168 = 64512); warpgroup 0 (producer,
   // MMA) drops to 80, the two softmax warpgroups rise to 208: 128*80 + 2*128*208 = 63488.
@@ -99,6 +108,26 @@ struct FwdCfg {
   static constexpr uint32_t BAR_P = 3;
   static constexpr uint32_t BAR_P_THREADS = 128 + 32 + 32;
 };
+
+// The normaliser block of a d = 64 forward: a [128 keys x 64 columns] bf16 tile, in the
+// 128-byte-swizzled layout of a V tile, whose first 16 columns are 1 and the rest 0.  Written by
+// the whole CTA before its first __syncthreads and made visible to the tensor core.
+__device__ __forceinline__ void fill_ones_block(uint8_t* blk) {
+  const uint4 ones = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = threadIdx.x; i < 128 * 8; i += blockDim.x) {
+    const int row = i >> 3, unit = i & 7;            // 16-byte unit (8 columns) of the row
+    *reinterpret_cast<uint4*>(blk + sw128_offset(row, unit * 8)) = (unit < 2) ? ones : zero;
+  }
+  fence_proxy_async_smem();
+}
+
+// B operand of O_t += P_t [V_j | 1] at d = 64: V_j's 64 columns at v_addr + off, and the next
+// 64-column chunk (of which the product reads 16) at the normaliser block ones_off bytes after
+// v_addr: the chunk stride (leading byte offset) is whatever separates the two.
+__device__ __forceinline__ uint64_t v_desc_ones(uint32_t v_addr, uint32_t off, uint32_t ones_off) {
+  return smem_desc_sw128(v_addr + off, ones_off - off, 1024);
+}
 
 // Registers the setmaxnreg split of a forward configuration needs: warpgroup 0 at REG_CTRL,
 // the two softmax warpgroups at REG_SOFTMAX.
@@ -242,6 +271,7 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
     tma_prefetch_desc(&p.tv);
     tma_prefetch_desc(&p.to);
   }
+  if constexpr (C::LB_MMA) fill_ones_block(smem + C::OFF_ONES);
   // Block-sparse: the CTA streams the key tiles either query tile wants (the union of its two
   // mask rows, in order; with causal only tiles up to the diagonal), once.  Both tiles run
   // every streamed tile; a tile whose block is not set masks it whole (P = 0).
@@ -337,7 +367,7 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       const bool leader = lane == 0;
       // Q, K both K-major; P from TMEM, V MN-major
       const uint32_t idesc_s = F8 ? idesc_e4m3_f32(128, 128, 0, 0) : idesc_bf16_f32(128, 128, 0, 0);
-      const uint32_t idesc_o = F8 ? idesc_e4m3_f32(128, D, 0, 1) : idesc_bf16_f32(128, D, 0, 1);
+      const uint32_t idesc_o = F8 ? idesc_e4m3_f32(128, D, 0, 1) : idesc_bf16_f32(128, C::DO, 0, 1);
       // Descriptors are built once; each k-step adds a compile-time offset (desc_advance).
       const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 0, 1024);
       const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 0, 1024);
@@ -359,8 +389,9 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
         umma_commit(&s_full[t]);
       };
       auto issue_pv = [&](int t, int j, bool first) {           // O_t += P_t V_j
-        const uint64_t b = desc_advance(dv0, (j % C::NS) * C::TILE);
-        const uint32_t d_tmem = tbase + C::T_O + t * D;
+        const uint64_t b = C::LB_MMA ? v_desc_ones(smem_u32(sV), (j % C::NS) * C::TILE, C::NS * C::TILE)
+                                     : desc_advance(dv0, (j % C::NS) * C::TILE);
+        const uint32_t d_tmem = tbase + C::T_O + t * C::DO;
         const uint32_t a_tmem = tbase + C::T_S + t * 128;
 #pragma unroll
         for (int ks = 0; ks < C::KS_PV; ++ks) {
@@ -435,7 +466,7 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
     if (lane == 0 && n_max > 0) {
       // Q, K both K-major; P from TMEM, V MN-major
       const uint32_t idesc_s = F8 ? idesc_e4m3_f32(128, 128, 0, 0) : idesc_bf16_f32(128, 128, 0, 0);
-      const uint32_t idesc_o = F8 ? idesc_e4m3_f32(128, D, 0, 1) : idesc_bf16_f32(128, D, 0, 1);
+      const uint32_t idesc_o = F8 ? idesc_e4m3_f32(128, D, 0, 1) : idesc_bf16_f32(128, C::DO, 0, 1);
       // Descriptors are built once; each k-step adds a compile-time offset (desc_advance).
       const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 0, 1024);
       const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 0, 1024);
@@ -457,8 +488,9 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
         umma_commit(&s_full[t]);
       };
       auto issue_pv = [&](int t, int j, bool first) {           // O_t += P_t V_j
-        const uint64_t b = desc_advance(dv0, (j % C::NS) * C::TILE);
-        const uint32_t d_tmem = tbase + C::T_O + t * D;
+        const uint64_t b = C::LB_MMA ? v_desc_ones(smem_u32(sV), (j % C::NS) * C::TILE, C::NS * C::TILE)
+                                     : desc_advance(dv0, (j % C::NS) * C::TILE);
+        const uint32_t d_tmem = tbase + C::T_O + t * C::DO;
         const uint32_t a_tmem = tbase + C::T_S + t * 128;
 #pragma unroll
         for (int ks = 0; ks < C::KS_PV; ++ks) {
@@ -572,7 +604,7 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
     const int row = sub * 32 + lane;
     const uint32_t t_lane = static_cast<uint32_t>(sub * 32) << 16;
     const uint32_t t_s = tbase + t_lane + C::T_S + t * 128;
-    const uint32_t t_o = tbase + t_lane + C::T_O + t * D;
+    const uint32_t t_o = tbase + t_lane + C::T_O + t * C::DO;
     const int q0t = q0[t];                    // this warpgroup's tile, hoisted out of the arrays
     const int lo_t = WIN ? lo[t] : 0;
     const int q_idx = q0t + row;
@@ -660,6 +692,14 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
             }
             tmem_st32(t_o + k * 32, rr);
           }
+          if constexpr (C::LB_MMA) {            // the normaliser columns move with O
+            uint32_t rr[16];
+            tmem_ld16(t_o + D, rr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * alpha);
+            tmem_st16(t_o + D, rr);
+          }
         }
       }
       const float ms = (m == -INFINITY) ? 0.f : m * c2 - C::P_BIAS;
@@ -694,8 +734,9 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
           pk[k] = pack_bf16x2(p0, p1);
           rs[k & 3] = fadd2(rs[k & 3], make_float2(p0, p1));
           // lb sums the bf16 weights the PV product uses, so O / lb is an exact weighted
-          // average of V under those weights; lse keeps the fp32 sum
-          rb[k & 3] = add_bf16x2_f32(rb[k & 3], pk[k]);
+          // average of V under those weights; lse keeps the fp32 sum (d = 64: the tensor core
+          // forms lb in O's normaliser columns)
+          if constexpr (!C::LB_MMA) rb[k & 3] = add_bf16x2_f32(rb[k & 3], pk[k]);
         }
         tmem_st32(t_s + h * 32, pk);
       }
@@ -734,6 +775,14 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
     const bool rowwise = VL && (q0[t] + C::BM > n_q);
     uint16_t* orow = rowwise ? p.o + (static_cast<size_t>(q_beg + q_idx) * p.heads + head) * D : nullptr;
     if (ok && q0[t] < n_q) {
+      if constexpr (C::LB_MMA) {               // the normaliser: O_t's column d
+        uint32_t rl[16];
+        if (n > 0) {
+          tmem_ld16(t_o + D, rl);
+          tmem_wait_ld();
+          lb = __uint_as_float(rl[0]);
+        }
+      }
       const float inv_l = F8 ? ((l > 0.f) ? p.out_scale / l : 0.f) : ((lb > 0.f) ? 1.f / lb : 0.f);
 #pragma unroll
       for (int k = 0; k < D / 32; ++k) {
@@ -817,7 +866,11 @@ struct FwdPCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = 2 * TILE;
   static constexpr int OFF_V = OFF_K + NS * TILE;
-  static constexpr int OFF_OST = OFF_V + NS * TILE;   // one O tile of staging, the tiles in turn
+  // d = 64: O's normaliser columns against a block of ones right after the V ring (as fwd_kernel)
+  static constexpr bool LB_MMA = D == 64;
+  static constexpr int DO = LB_MMA ? D + 16 : D;      // TMEM columns of O_t
+  static constexpr int OFF_ONES = OFF_V + NS * TILE;
+  static constexpr int OFF_OST = OFF_ONES + (LB_MMA ? CHUNK : 0);   // one O tile of staging
   static constexpr int OFF_BAR = OFF_OST + TILE;
   // q_full, q_empty, k_full[NS], k_empty[NS], v_full[NS], v_empty[NS], s_full[2], p_full[2],
   // o_done[2], o_free[2], st_free
@@ -909,6 +962,7 @@ fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
     tma_prefetch_desc(&p.tv);
     tma_prefetch_desc(&p.to);
   }
+  if constexpr (C::LB_MMA) fill_ones_block(smem + C::OFF_ONES);
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   __syncthreads();
   tc_fence_after();
@@ -959,7 +1013,7 @@ fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
-      const uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
+      const uint32_t idesc_o = idesc_bf16_f32(128, C::DO, 0, 1);
       const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 0, 1024);
       const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 0, 1024);
       const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), C::CHUNK, 1024);
@@ -976,10 +1030,11 @@ fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
         umma_commit(&s_full[t]);
       };
       auto issue_pv = [&](int t, uint32_t P, bool first) {     // O_t += P_t V (position P)
-        const uint64_t b = desc_advance(dv0, (P % C::NS) * C::TILE);
+        const uint64_t b = C::LB_MMA ? v_desc_ones(smem_u32(sV), (P % C::NS) * C::TILE, C::NS * C::TILE)
+                                     : desc_advance(dv0, (P % C::NS) * C::TILE);
 #pragma unroll
         for (int ks = 0; ks < C::KS_PV; ++ks)
-          umma_ts(tbase + C::T_O + t * D, tbase + C::T_S + t * 128 + ks * 8,
+          umma_ts(tbase + C::T_O + t * C::DO, tbase + C::T_S + t * 128 + ks * 8,
                   desc_advance(b, ks * 16 * 128), idesc_o, (!first || ks > 0) ? 1u : 0u);
       };
       uint32_t P = 0, cp[2] = {0, 0}, act[2] = {0, 0};
@@ -1057,7 +1112,7 @@ fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
     const int row = sub * 32 + lane;
     const uint32_t t_lane = static_cast<uint32_t>(sub * 32) << 16;
     const uint32_t t_s = tbase + t_lane + C::T_S + t * 128;
-    const uint32_t t_o = tbase + t_lane + C::T_O + t * D;
+    const uint32_t t_o = tbase + t_lane + C::T_O + t * C::DO;
     const float c2 = p.scale_log2;
     const float2 c2v = make_float2(c2, c2);
     uint32_t cs = 0, act = 0, uses = 0;       // S hand-offs, items of this tile, staging uses
@@ -1112,7 +1167,7 @@ fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
           }
           if (j > 0) {                          // O_t settled: PV_t(j-1) preceded S_t(j)
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {  // 16 columns at a time (s[] is live here)
+            for (int kk = 0; kk < C::DO / 16; ++kk) {  // 16 columns at a time (s[] is live here)
               uint32_t rr[16];
               tmem_ld16(t_o + kk * 16, rr);
               tmem_wait_ld();
@@ -1140,8 +1195,9 @@ fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
             const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
             pk[kk] = pack_bf16x2(p0, p1);
             rs[kk & 3] = fadd2(rs[kk & 3], make_float2(p0, p1));
-            // lb sums the bf16 weights the PV product uses (O / lb is their exact average)
-            rb[kk & 3] = add_bf16x2_f32(rb[kk & 3], pk[kk]);
+            // lb sums the bf16 weights the PV product uses (O / lb is their exact average);
+            // d = 64: the tensor core forms it in O's normaliser columns
+            if constexpr (!C::LB_MMA) rb[kk & 3] = add_bf16x2_f32(rb[kk & 3], pk[kk]);
           }
           tmem_st32(t_s + h * 32, pk);
         }
@@ -1162,6 +1218,12 @@ fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
       if (ok && my_use > 0) ok = mbar_wait_warp(st_free, (my_use - 1) & 1, abort_flag, 173);
       if (ok) {
         tc_fence_after();
+        if constexpr (C::LB_MMA) {             // the normaliser: O_t's column d
+          uint32_t rl[16];
+          tmem_ld16(t_o + D, rl);
+          tmem_wait_ld();
+          lb = __uint_as_float(rl[0]);
+        }
         const float inv_l = (lb > 0.f) ? 1.f / lb : 0.f;
 #pragma unroll
         for (int kk = 0; kk < D / 32; ++kk) {
