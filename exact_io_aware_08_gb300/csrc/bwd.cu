@@ -66,7 +66,11 @@ struct BwdCfg {
   // d = 128: staging of one fp32 dQ tile [BM queries][d] for the TMA reduce-add into dQ_acc
   static constexpr int DQS_BYTES = (D == 128) ? BM * D * 4 : 0;
   static constexpr int OFF_DQS = OFF_DS + 2 * DS_TILE;      // dS^T double-buffered
-  static constexpr int OFF_BAR = OFF_DQS + DQS_BYTES;
+  // d = 128: one 32-float slot per dS warp, through which its lanes pass the step's -lse and
+  // then -D to the whole warp (broadcast loads instead of shuffles)
+  static constexpr int OFF_SLOT = OFF_DQS + DQS_BYTES;
+  static constexpr int SLOT_BYTES = (D == 128) ? 8 * 32 * 4 : 0;
+  static constexpr int OFF_BAR = OFF_SLOT + SLOT_BYTES;
   // kv_full, stage_full[NST], stage_empty[NST], st_full, dp_full, p_ready, ds_ready,
   // pds_free[2], dq_full[2], dq_free[2], mma_done, dqs_sync, dqs_done[2]
   static constexpr int NBAR = 1 + 2 * NST + 14;
@@ -424,8 +428,19 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       // folded in by the helper); dp_full(i), waited for below: dP_i is done
       if (!(ok = mbar_wait_warp(st_full, i & 1, abort_flag, 221))) break;
       tc_fence_after();
+      float* slot = reinterpret_cast<float*>(smem + C::OFF_SLOT) + (warp - 2) * 32;
+      if constexpr (D == 128) {
+        slot[lane] = lane_nl;
+        __syncwarp();
 #pragma unroll
-      for (int e = 0; e < 32; ++e) nl0[e] = __shfl_sync(0xffffffffu, lane_nl, e);
+        for (int e = 0; e < 32; e += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(slot + e);
+          nl0[e] = v.x; nl0[e + 1] = v.y; nl0[e + 2] = v.z; nl0[e + 3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) nl0[e] = __shfl_sync(0xffffffffu, lane_nl, e);
+      }
       // a (key tile, query tile) pair that some pair of rows sees only in part
       const bool diag = WIN ? ((q0 < k0 + C::BN - 1 - wr) || (q0 + C::BM - 1 > k0 + wl))
                             : (p.causal && (q0 < k0 + C::BN - 1));
@@ -498,12 +513,22 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_ready);
+      if constexpr (D == 128) {                    // the slot now passes -D (nl0 was read out)
+        __syncwarp();
+        slot[lane] = lane_nd[0];
+        __syncwarp();
+      }
       // dS^T = P^T o (dP^T - D)
 #pragma unroll
       for (int e = 0; e < C::HALF; e += 2) {
         const float2 dp = make_float2(__uint_as_float(dpu[e / 32][e % 32]), __uint_as_float(dpu[e / 32][e % 32 + 1]));
-        const float2 nd = make_float2(__shfl_sync(0xffffffffu, lane_nd[e / 32], e % 32),
-                                      __shfl_sync(0xffffffffu, lane_nd[e / 32], e % 32 + 1));
+        float2 nd;
+        if constexpr (D == 128) {
+          nd = *reinterpret_cast<const float2*>(slot + e);
+        } else {
+          nd = make_float2(__shfl_sync(0xffffffffu, lane_nd[e / 32], e % 32),
+                           __shfl_sync(0xffffffffu, lane_nd[e / 32], e % 32 + 1));
+        }
         float2 pp;
         if constexpr (kPackedP)
           pp = make_float2(__uint_as_float(ppk[e / 2] << 16), __uint_as_float(ppk[e / 2] & 0xffff0000u));
