@@ -66,10 +66,10 @@ struct BwdCfg {
   // d = 128: staging of one fp32 dQ tile [BM queries][d] for the TMA reduce-add into dQ_acc
   static constexpr int DQS_BYTES = (D == 128) ? BM * D * 4 : 0;
   static constexpr int OFF_DQS = OFF_DS + 2 * DS_TILE;      // dS^T double-buffered
-  // d = 128: one 32-float slot per dS warp, through which its lanes pass the step's -lse and
-  // then -D to the whole warp (broadcast loads instead of shuffles)
+  // one slot of HALF floats per dS warp, through which its lanes pass the step's -lse and then
+  // -D to the whole warp (broadcast loads instead of shuffles)
   static constexpr int OFF_SLOT = OFF_DQS + DQS_BYTES;
-  static constexpr int SLOT_BYTES = (D == 128) ? 8 * 32 * 4 : 0;
+  static constexpr int SLOT_BYTES = 8 * (BM / 2) * 4;
   static constexpr int OFF_BAR = OFF_SLOT + SLOT_BYTES;
   // kv_full, stage_full[NST], stage_empty[NST], st_full, dp_full, p_ready, ds_ready,
   // pds_free[2], dq_full[2], dq_free[2], mma_done, dqs_sync, dqs_done[2]
@@ -428,18 +428,13 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       // folded in by the helper); dp_full(i), waited for below: dP_i is done
       if (!(ok = mbar_wait_warp(st_full, i & 1, abort_flag, 221))) break;
       tc_fence_after();
-      float* slot = reinterpret_cast<float*>(smem + C::OFF_SLOT) + (warp - 2) * 32;
-      if constexpr (D == 128) {
-        slot[lane] = lane_nl;
-        __syncwarp();
+      float* slot = reinterpret_cast<float*>(smem + C::OFF_SLOT) + (warp - 2) * C::HALF;
+      slot[lane] = lane_nl;
+      __syncwarp();
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 v = *reinterpret_cast<const float4*>(slot + e);
-          nl0[e] = v.x; nl0[e + 1] = v.y; nl0[e + 2] = v.z; nl0[e + 3] = v.w;
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) nl0[e] = __shfl_sync(0xffffffffu, lane_nl, e);
+      for (int e = 0; e < 32; e += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(slot + e);
+        nl0[e] = v.x; nl0[e + 1] = v.y; nl0[e + 2] = v.z; nl0[e + 3] = v.w;
       }
       // a (key tile, query tile) pair that some pair of rows sees only in part
       const bool diag = WIN ? ((q0 < k0 + C::BN - 1 - wr) || (q0 + C::BM - 1 > k0 + wl))
@@ -472,10 +467,14 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
 #pragma unroll
           for (int e = 0; e < 32; ++e) nl[e] = nl0[e];
         } else {
-          const float lane_nl_c = nlse_of(q0 + cb + c * 32 + lane);
+          slot[c * 32 + lane] = nlse_of(q0 + cb + c * 32 + lane);
           lane_nd[c] = nd_of(q0 + cb + c * 32 + lane);
+          __syncwarp();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) nl[e] = __shfl_sync(0xffffffffu, lane_nl_c, e);
+          for (int e = 0; e < 32; e += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(slot + c * 32 + e);
+            nl[e] = v.x; nl[e + 1] = v.y; nl[e + 2] = v.z; nl[e + 3] = v.w;
+          }
         }
         tmem_wait_ld();
         uint32_t pk_p[16];
@@ -513,22 +512,15 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_ready);
-      if constexpr (D == 128) {                    // the slot now passes -D (nl0 was read out)
-        __syncwarp();
-        slot[lane] = lane_nd[0];
-        __syncwarp();
-      }
+      __syncwarp();                                // the slot now passes -D (-lse was read out)
+#pragma unroll
+      for (int c = 0; c < C::HALF / 32; ++c) slot[c * 32 + lane] = lane_nd[c];
+      __syncwarp();
       // dS^T = P^T o (dP^T - D)
 #pragma unroll
       for (int e = 0; e < C::HALF; e += 2) {
         const float2 dp = make_float2(__uint_as_float(dpu[e / 32][e % 32]), __uint_as_float(dpu[e / 32][e % 32 + 1]));
-        float2 nd;
-        if constexpr (D == 128) {
-          nd = *reinterpret_cast<const float2*>(slot + e);
-        } else {
-          nd = make_float2(__shfl_sync(0xffffffffu, lane_nd[e / 32], e % 32),
-                           __shfl_sync(0xffffffffu, lane_nd[e / 32], e % 32 + 1));
-        }
+        const float2 nd = *reinterpret_cast<const float2*>(slot + e);
         float2 pp;
         if constexpr (kPackedP)
           pp = make_float2(__uint_as_float(ppk[e / 2] << 16), __uint_as_float(ppk[e / 2] & 0xffff0000u));
@@ -758,7 +750,8 @@ struct BwdP64 {
   static constexpr int OFF_V = 2 * B::KV_TILE;
   static constexpr int OFF_ST = 3 * B::KV_TILE;         // Q, dO ring
   static constexpr int OFF_DS = OFF_ST + NST * B::STAGE;
-  static constexpr int OFF_BAR = OFF_DS + 2 * B::DS_TILE;
+  static constexpr int OFF_SLOT = OFF_DS + 2 * B::DS_TILE;   // -lse / -D slots (bwd_main_kernel)
+  static constexpr int OFF_BAR = OFF_SLOT + 8 * HALF * 4;
   // k_full[2], k_free[2], v_full, v_free, stage_full[NST], stage_empty[NST], st_full, dp_full,
   // p_ready, ds_ready, dq_full[2], dq_free[2], acc_full, acc_free, mma_done, dqs_sync,
   // dqs_done[2]
@@ -1050,8 +1043,15 @@ bwd_persistent_kernel64(const __grid_constant__ BwdParams p) {
         lane_nd[0] = nd_of(q0 + cb + lane);
         if (!(ok = mbar_wait_warp(st_full, g & 1, abort_flag, 321))) break;
         tc_fence_after();
+        // -lse, then -D, pass to the whole warp through its slot (as in bwd_main_kernel)
+        float* slot = reinterpret_cast<float*>(smem + C::OFF_SLOT) + (warp - 2) * C::HALF;
+        slot[lane] = lane_nl;
+        __syncwarp();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) nl0[e] = __shfl_sync(0xffffffffu, lane_nl, e);
+        for (int e = 0; e < 32; e += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(slot + e);
+          nl0[e] = v.x; nl0[e + 1] = v.y; nl0[e + 2] = v.z; nl0[e + 3] = v.w;
+        }
         const bool diag = p.causal && (q0 < k0 + C::BN - 1);
         uint32_t pk_ds[C::HALF / 2];
         uint32_t ppk[C::HALF / 2];                   // P as bf16 pairs (see bwd_main_kernel)
@@ -1065,10 +1065,14 @@ bwd_persistent_kernel64(const __grid_constant__ BwdParams p) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) nl[e] = nl0[e];
           } else {
-            const float lane_nl_c = nlse_of(q0 + cb + cc * 32 + lane);
+            slot[cc * 32 + lane] = nlse_of(q0 + cb + cc * 32 + lane);
             lane_nd[cc] = nd_of(q0 + cb + cc * 32 + lane);
+            __syncwarp();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) nl[e] = __shfl_sync(0xffffffffu, lane_nl_c, e);
+            for (int e = 0; e < 32; e += 4) {
+              const float4 v = *reinterpret_cast<const float4*>(slot + cc * 32 + e);
+              nl[e] = v.x; nl[e + 1] = v.y; nl[e + 2] = v.z; nl[e + 3] = v.w;
+            }
           }
           tmem_wait_ld();
           uint32_t pk_p[16];
@@ -1093,11 +1097,14 @@ bwd_persistent_kernel64(const __grid_constant__ BwdParams p) {
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(p_ready);
+        __syncwarp();                              // the slot now passes -D
+#pragma unroll
+        for (int cc = 0; cc < C::HALF / 32; ++cc) slot[cc * 32 + lane] = lane_nd[cc];
+        __syncwarp();
 #pragma unroll
         for (int e = 0; e < C::HALF; e += 2) {
           const float2 dp = make_float2(__uint_as_float(dpu[e / 32][e % 32]), __uint_as_float(dpu[e / 32][e % 32 + 1]));
-          const float2 nd = make_float2(__shfl_sync(0xffffffffu, lane_nd[e / 32], e % 32),
-                                        __shfl_sync(0xffffffffu, lane_nd[e / 32], e % 32 + 1));
+          const float2 nd = *reinterpret_cast<const float2*>(slot + e);
           const float2 pp = make_float2(__uint_as_float(ppk[e / 2] << 16), __uint_as_float(ppk[e / 2] & 0xffff0000u));
           const float2 ds = fmul2(pp, fadd2(dp, nd));
           pk_ds[e / 2] = pack_bf16x2(ds.x, ds.y);
