@@ -312,7 +312,11 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n > 0) {
+    // d = 64: the converged warp issues (umma_*_w); d = 128: one thread (measured: the
+    // 4x32x4096x128 backward 2.49 ms against 2.52 ms with the warp, 4x16x2048x64 272 against
+    // 279 us the other way)
+    constexpr bool WI = D == 64;
+    if ((WI || lane == 0) && n > 0) {
       const uint32_t id_s = idesc_bf16_f32(128, C::BM, 0, 0);     // K/V K-major, Q/dO K-major
       const uint32_t id_acc = idesc_bf16_f32(128, D, 0, 1);       // P^T (TMEM) / dS^T K-major, dO/Q MN-major
       const uint32_t id_dq = idesc_bf16_f32(128, 64, 1, 1);       // both MN-major
@@ -333,19 +337,19 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t kv_off = (ks >> 2) * C::KV_CHUNK + (ks & 3) * 32;
           const uint32_t q_off = (ks >> 2) * C::Q_CHUNK + (ks & 3) * 32;
-          umma_ss(tbase + C::T_S, desc_advance(dK_k, kv_off), desc_advance(q_k, q_off), id_s, ks > 0);
+          umma_ss_by<WI>(tbase + C::T_S, desc_advance(dK_k, kv_off), desc_advance(q_k, q_off), id_s, ks > 0);
         }
-        umma_commit(st_full);
+        umma_commit_by<WI>(st_full);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t kv_off = (ks >> 2) * C::KV_CHUNK + (ks & 3) * 32;
           const uint32_t q_off = (ks >> 2) * C::Q_CHUNK + (ks & 3) * 32;
-          umma_ss(tbase + C::T_DP, desc_advance(dV_k, kv_off), desc_advance(do_k, q_off), id_s, ks > 0);
+          umma_ss_by<WI>(tbase + C::T_DP, desc_advance(dV_k, kv_off), desc_advance(do_k, q_off), id_s, ks > 0);
         }
-        umma_commit(dp_full);
+        umma_commit_by<WI>(dp_full);
       };
-      bool ok = mbar_wait(kv_full, 0, abort_flag, 211) &&
-                mbar_wait(&stage_full[0], 0, abort_flag, 212);
+      bool ok = mbar_wait_by<WI>(kv_full, 0, abort_flag, 211) &&
+                mbar_wait_by<WI>(&stage_full[0], 0, abort_flag, 212);
       if (ok) {
         tc_fence_after();
         issue_s_dp(0);
@@ -357,22 +361,22 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
       // form dS_i, and dK_i/dQ_i while they start on step i+1.
       for (int i = 0; ok && i < n; ++i) {
         const int s = i % C::NST;
-        if (!(ok = mbar_wait(p_ready, i & 1, abort_flag, 215))) break;
+        if (!(ok = mbar_wait_by<WI>(p_ready, i & 1, abort_flag, 215))) break;
         tc_fence_after();
         const uint64_t q_mn = desc_advance(dST_mn, s * C::STAGE);
         const uint64_t do_mn = desc_advance(dST_mn, s * C::STAGE + C::Q_TILE);
 #pragma unroll
         for (int ks = 0; ks < C::BM / 16; ++ks)       // dV += P^T dO
-          umma_ts(tbase + C::T_DV, tbase + C::T_S + ks * 8 + ((16 * ks) / C::HALF) * (C::HALF / 2),
+          umma_ts_by<WI>(tbase + C::T_DV, tbase + C::T_S + ks * 8 + ((16 * ks) / C::HALF) * (C::HALF / 2),
                   desc_advance(do_mn, ks * 2048), id_acc, (i > 0 || ks > 0) ? 1u : 0u);
         // stage i+1 is loaded: p_ready(i) includes the helper's check of it
         if (i + 1 < n) issue_s_dp(i + 1);
-        if (!(ok = mbar_wait(ds_ready, i & 1, abort_flag, 218))) break;
+        if (!(ok = mbar_wait_by<WI>(ds_ready, i & 1, abort_flag, 218))) break;
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < C::BM / 16; ++ks) {     // dK += dS^T Q
           const uint32_t a_off = (ks >> 2) * C::KV_CHUNK + (ks & 3) * 32;
-          umma_ss(tbase + C::T_DK, desc_advance(dDS, (i & 1) * C::DS_TILE + a_off), desc_advance(q_mn, ks * 2048), id_acc,
+          umma_ss_by<WI>(tbase + C::T_DK, desc_advance(dDS, (i & 1) * C::DS_TILE + a_off), desc_advance(q_mn, ks * 2048), id_acc,
                   (i > 0 || ks > 0) ? 1u : 0u);
         }
         // dQ TMEM buffer of this step, drained: ds_ready(i) includes the helper's check of it
@@ -383,16 +387,16 @@ bwd_main_kernel(const __grid_constant__ BwdParams p) {
           // d = 64:  dQ   = dS K     (A = dS^T as MN-major, B = K as MN-major)
           const uint64_t kd = desc_advance(dK_mn, ks * 2048);
           const uint64_t dd = desc_advance(dDS_mn, (i & 1) * C::DS_TILE + ks * 2048);
-          if constexpr (D == 128) umma_ss(tbase + C::T_DQ + qb * 64, kd, dd, id_dq, ks > 0);
-          else umma_ss(tbase + C::T_DQ + qb * 64, dd, kd, id_dq, ks > 0);
+          if constexpr (D == 128) umma_ss_by<WI>(tbase + C::T_DQ + qb * 64, kd, dd, id_dq, ks > 0);
+          else umma_ss_by<WI>(tbase + C::T_DQ + qb * 64, dd, kd, id_dq, ks > 0);
         }
-        umma_commit(&dq_full[qb]);
-        if constexpr (D == 128) umma_commit(&pds_free[i & 1]);   // d = 64: dqs_done (dQ warps)
-        umma_commit(&stage_empty[s]);
+        umma_commit_by<WI>(&dq_full[qb]);
+        if constexpr (D == 128) umma_commit_by<WI>(&pds_free[i & 1]);   // d = 64: dqs_done (dQ warps)
+        umma_commit_by<WI>(&stage_empty[s]);
       }
-      umma_commit(mma_done);
-      mbar_wait(mma_done, 0, nullptr, 217);
-      if (ok && p.stats != nullptr) atomicAdd(&p.stats[1], static_cast<unsigned long long>(n));
+      umma_commit_by<WI>(mma_done);
+      mbar_wait_by<WI>(mma_done, 0, nullptr, 217);
+      if (ok && lane == 0 && p.stats != nullptr) atomicAdd(&p.stats[1], static_cast<unsigned long long>(n));
     }
   } else if (warp < 10) {
     // ------------------------------------------------------------------ dS warpgroups
@@ -913,6 +917,8 @@ bwd_persistent_kernel64(const __grid_constant__ BwdParams p) {
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
+    // one thread issues (measured: the GPT-2-medium layer backward 125 us, 135 us when the
+    // converged warp issues)
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(128, C::BM, 0, 0);
       const uint32_t id_acc = idesc_bf16_f32(128, D, 0, 1);
@@ -1260,11 +1266,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
                                                       const uint16_t* __restrict__ dO,
                                                       float* __restrict__ delta,
                                                       float4* __restrict__ dq_acc4,
-                                                      long long rows, long long acc4, int vl_heads) {
+                                                      long long rows, int vl_heads) {
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long nthr = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long x = tid; x < acc4; x += nthr) dq_acc4[x] = make_float4(0.f, 0.f, 0.f, 0.f);
   constexpr int TPR = D / 8;                        // threads per row, 8 bf16 each
+  static_assert(D / 4 == 2 * TPR, "a thread clears two float4 of its row's accumulator");
   constexpr int RPW = 32 / TPR;                     // rows per warp and pass
   const int lane = threadIdx.x & 31;
   const int part = lane % TPR;
@@ -1277,6 +1283,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint16_t* __restrict
     if (valid) {
       const uint4 a = __ldg(reinterpret_cast<const uint4*>(o + row * D) + part);
       const uint4 b = __ldg(reinterpret_cast<const uint4*>(dO + row * D) + part);
+      // the row's fp32 dQ accumulator is cleared beside the reads: one mixed read/write stream
+      // instead of a write-only pass and then a read-only pass (4x32x4096x128: 93 against 107 us)
+      float4* z = dq_acc4 + row * (D / 4) + part * 2;
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
       const uint32_t aa[4] = {a.x, a.y, a.z, a.w}, bb[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -1309,12 +1320,11 @@ static cudaError_t launch_bwd_prep_d(const BwdArgs& a, cudaStream_t stream) {
   const uint64_t bh = static_cast<uint64_t>(a.B) * a.H;
   const long long rows = static_cast<long long>(bh) * a.n_q;
   if (rows == 0) return cudaSuccess;
-  const long long acc4 = rows * D / 4;
   const int blocks = static_cast<int>(std::min<long long>(152LL * 8, (rows * (D / 8) + 255) / 256));
   log_launch("bwd_pre_kernel<D>", static_cast<unsigned long long>(std::max(blocks, 1)), 256, static_cast<unsigned long long>(0));
   bwd_pre_kernel<D><<<std::max(blocks, 1), 256, 0, stream>>>(
       static_cast<const uint16_t*>(a.o), static_cast<const uint16_t*>(a.dO), a.delta,
-      reinterpret_cast<float4*>(a.dq_acc), rows, acc4, a.cu_q != nullptr ? a.H : 0);
+      reinterpret_cast<float4*>(a.dq_acc), rows, a.cu_q != nullptr ? a.H : 0);
   return cudaGetLastError();
 }
 

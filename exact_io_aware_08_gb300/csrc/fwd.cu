@@ -9,7 +9,8 @@
 // GB300 mapping.  One CTA (384 threads, one per SM) owns TWO 128-row query tiles of a head,
 // which share every K/V tile loaded into shared memory:
 //   warp 0      TMA producer: Q_0, Q_1 once, then K_j and V_j through NS-deep rings.
-//   warp 1      TMEM owner and single-thread MMA issuer (tcgen05.mma kind::f16, fp32 in TMEM):
+//   warp 1      TMEM owner and MMA issuer, the whole warp converged with one elected lane
+//               issuing (tcgen05.mma kind::f16, fp32 in TMEM):
 //                 S_t = Q_t K_j^T          A, B from shared memory (both K-major)
 //                 O_t += P_t V_j           A = P_t from TMEM, B = V_j from shared memory
 //               in the order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so the tensor core works
@@ -361,8 +362,8 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
     }
   } else if (C::NAMED_P && warp == 1) {
     // ------------------------------------------------------------------ MMA issuer (fp8)
-    // The whole warp walks the loop (it takes part in the named-barrier hand-offs); lane 0
-    // issues.  After a failed wait the warp keeps joining every hand-off, issuing nothing.
+    // The whole warp walks the loop (it takes part in the named-barrier hand-offs) and issues
+    // (umma_*_w).  After a failed wait it keeps joining every hand-off, issuing nothing.
     if (n_max > 0) {
       const bool leader = lane == 0;
       // Q, K both K-major; P from TMEM, V MN-major
@@ -382,11 +383,11 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
         for (int ks = 0; ks < C::KS_S; ++ks) {
           const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
           if constexpr (F8)
-            umma_ss_f8(d_tmem, desc_advance(a, off), desc_advance(b, off), idesc_s, ks > 0);
+            umma_ss_f8_w(d_tmem, desc_advance(a, off), desc_advance(b, off), idesc_s, ks > 0);
           else
-            umma_ss(d_tmem, desc_advance(a, off), desc_advance(b, off), idesc_s, ks > 0);
+            umma_ss_w(d_tmem, desc_advance(a, off), desc_advance(b, off), idesc_s, ks > 0);
         }
-        umma_commit(&s_full[t]);
+        umma_commit_w(&s_full[t]);
       };
       auto issue_pv = [&](int t, int j, bool first) {           // O_t += P_t V_j
         const uint64_t b = C::LB_MMA ? v_desc_ones(smem_u32(sV), (j % C::NS) * C::TILE, C::NS * C::TILE)
@@ -396,19 +397,19 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
 #pragma unroll
         for (int ks = 0; ks < C::KS_PV; ++ks) {
           if constexpr (F8)
-            umma_ts_f8(d_tmem, a_tmem + ks * 8, desc_advance(b, ks * C::PV_B_STEP), idesc_o,
+            umma_ts_f8_w(d_tmem, a_tmem + ks * 8, desc_advance(b, ks * C::PV_B_STEP), idesc_o,
                        (!first || ks > 0) ? 1u : 0u);
           else
-            umma_ts(d_tmem, a_tmem + ks * 8, desc_advance(b, ks * C::PV_B_STEP), idesc_o,
+            umma_ts_w(d_tmem, a_tmem + ks * 8, desc_advance(b, ks * C::PV_B_STEP), idesc_o,
                     (!first || ks > 0) ? 1u : 0u);
         }
       };
       bool ok = mbar_wait_warp(q_full, 0, abort_flag, 111) && mbar_wait_warp(&k_full[0], 0, abort_flag, 112);
-      if (ok && leader) {
+      if (ok) {
         tc_fence_after();
         if (n_t[0] > 0) issue_s(0, 0);
         if (n_t[1] > 0 && (!WIN || off[1] == 0)) issue_s(1, 0);
-        umma_commit(&k_empty[0]);
+        umma_commit_w(&k_empty[0]);
       }
       // stream position j; tile t is on its i-th key tile, i = j - off[t]
       for (int j = 0; j < n_max; ++j) {
@@ -420,17 +421,17 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
           if ((!WIN || i >= 0) && i < n_t[t]) {
             __syncwarp();
             named_bar_sync(C::BAR_P + t, C::BAR_P_THREADS);
-            if (ok && leader) {
+            if (ok) {
               tc_fence_after();
               issue_pv(t, j, i == 0);
-              if (i + 1 == n_t[t]) umma_commit(&o_done[t]);
+              if (i + 1 == n_t[t]) umma_commit_w(&o_done[t]);
             }
           }
-          if (ok && leader && (!WIN || i + 1 >= 0) && i + 1 < n_t[t]) issue_s(t, j + 1);
+          if (ok && (!WIN || i + 1 >= 0) && i + 1 < n_t[t]) issue_s(t, j + 1);
         }
-        if (ok && leader) {
-          umma_commit(&v_empty[s]);
-          if (j + 1 < n_max) umma_commit(&k_empty[(j + 1) % C::NS]);
+        if (ok) {
+          umma_commit_w(&v_empty[s]);
+          if (j + 1 < n_max) umma_commit_w(&k_empty[(j + 1) % C::NS]);
         }
       }
       if (leader && p.stats != nullptr) atomicAdd(&p.stats[0], n_s);
@@ -463,7 +464,7 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_max > 0) {
+    if (n_max > 0) {                               // the whole warp (umma_*_w)
       // Q, K both K-major; P from TMEM, V MN-major
       const uint32_t idesc_s = F8 ? idesc_e4m3_f32(128, 128, 0, 0) : idesc_bf16_f32(128, 128, 0, 0);
       const uint32_t idesc_o = F8 ? idesc_e4m3_f32(128, D, 0, 1) : idesc_bf16_f32(128, C::DO, 0, 1);
@@ -481,11 +482,11 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
         for (int ks = 0; ks < C::KS_S; ++ks) {
           const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
           if constexpr (F8)
-            umma_ss_f8(d_tmem, desc_advance(a, off), desc_advance(b, off), idesc_s, ks > 0);
+            umma_ss_f8_w(d_tmem, desc_advance(a, off), desc_advance(b, off), idesc_s, ks > 0);
           else
-            umma_ss(d_tmem, desc_advance(a, off), desc_advance(b, off), idesc_s, ks > 0);
+            umma_ss_w(d_tmem, desc_advance(a, off), desc_advance(b, off), idesc_s, ks > 0);
         }
-        umma_commit(&s_full[t]);
+        umma_commit_w(&s_full[t]);
       };
       auto issue_pv = [&](int t, int j, bool first) {           // O_t += P_t V_j
         const uint64_t b = C::LB_MMA ? v_desc_ones(smem_u32(sV), (j % C::NS) * C::TILE, C::NS * C::TILE)
@@ -495,14 +496,14 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
 #pragma unroll
         for (int ks = 0; ks < C::KS_PV; ++ks) {
           if constexpr (F8)
-            umma_ts_f8(d_tmem, a_tmem + ks * 8, desc_advance(b, ks * C::PV_B_STEP), idesc_o,
+            umma_ts_f8_w(d_tmem, a_tmem + ks * 8, desc_advance(b, ks * C::PV_B_STEP), idesc_o,
                        (!first || ks > 0) ? 1u : 0u);
           else
-            umma_ts(d_tmem, a_tmem + ks * 8, desc_advance(b, ks * C::PV_B_STEP), idesc_o,
+            umma_ts_w(d_tmem, a_tmem + ks * 8, desc_advance(b, ks * C::PV_B_STEP), idesc_o,
                     (!first || ks > 0) ? 1u : 0u);
         }
       };
-      bool ok = mbar_wait(q_full, 0, abort_flag, 111) && mbar_wait(&k_full[0], 0, abort_flag, 112);
+      bool ok = mbar_wait_warp(q_full, 0, abort_flag, 111) && mbar_wait_warp(&k_full[0], 0, abort_flag, 112);
       if constexpr (BS) {
         // Only live (tile, block) pairs are computed; cnt[t] counts tile t's live steps.  An
         // S_t(j+1) of a tile that is clear at j waits for the other tile's hand-off at j, which
@@ -513,7 +514,7 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
 #pragma unroll
           for (int t = 0; t < 2; ++t)
             if (live(t, 0)) issue_s(t, 0);
-          umma_commit(&k_empty[0]);
+          umma_commit_w(&k_empty[0]);
         }
         for (int j = 0; ok && j < n_max; ++j) {
           const int s = j % C::NS;
@@ -523,11 +524,11 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (live(t, j)) {
-              if (!(ok = mbar_wait(&p_full[t], cnt[t] & 1, abort_flag, 115 + t))) break;
+              if (!(ok = mbar_wait_warp(&p_full[t], cnt[t] & 1, abort_flag, 115 + t))) break;
               tc_fence_after();
               waited = true;
               issue_pv(t, j, cnt[t] == 0);
-              if (++cnt[t] == n_t[t]) umma_commit(&o_done[t]);
+              if (++cnt[t] == n_t[t]) umma_commit_w(&o_done[t]);
             }
             if (nxt && live(t, j + 1)) {
               if (waited) issue_s(t, j + 1);
@@ -536,15 +537,15 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
           }
           if (!ok) break;
           if (deferred >= 0) issue_s(deferred, j + 1);
-          umma_commit(&v_empty[s]);
-          if (nxt) umma_commit(&k_empty[(j + 1) % C::NS]);
+          umma_commit_w(&v_empty[s]);
+          if (nxt) umma_commit_w(&k_empty[(j + 1) % C::NS]);
         }
       }
       if (!BS && ok) {
         tc_fence_after();
         if (n_t[0] > 0) issue_s(0, 0);
         if (n_t[1] > 0 && (!WIN || off[1] == 0)) issue_s(1, 0);
-        umma_commit(&k_empty[0]);
+        umma_commit_w(&k_empty[0]);
       }
       // stream position j; tile t is on its i-th key tile, i = j - off[t]
       for (int j = 0; !BS && ok && j < n_max; ++j) {
@@ -554,18 +555,18 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
         for (int t = 0; t < 2; ++t) {
           const int i = WIN ? j - off[t] : j;       // without a window both tiles start at 0
           if ((!WIN || i >= 0) && i < n_t[t]) {
-            if (!(ok = mbar_wait(&p_full[t], i & 1, abort_flag, 115 + t))) break;
+            if (!(ok = mbar_wait_warp(&p_full[t], i & 1, abort_flag, 115 + t))) break;
             tc_fence_after();
             issue_pv(t, j, i == 0);
-            if (i + 1 == n_t[t]) umma_commit(&o_done[t]);
+            if (i + 1 == n_t[t]) umma_commit_w(&o_done[t]);
           }
           if ((!WIN || i + 1 >= 0) && i + 1 < n_t[t]) issue_s(t, j + 1);
         }
         if (!ok) break;
-        umma_commit(&v_empty[s]);
-        if (j + 1 < n_max) umma_commit(&k_empty[(j + 1) % C::NS]);
+        umma_commit_w(&v_empty[s]);
+        if (j + 1 < n_max) umma_commit_w(&k_empty[(j + 1) % C::NS]);
       }
-      if (p.stats != nullptr) atomicAdd(&p.stats[0], n_s);
+      if (lane == 0 && p.stats != nullptr) atomicAdd(&p.stats[0], n_s);
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------------ helper
@@ -848,10 +849,13 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
 // ------------------------------------------------------------------------------------------
 // Heads short enough for the persistent forward: it pays when a work item is a few tiles long
 // (measured on GB300: up to 16 key tiles for causal heads, whose items average half the head,
-// and for d = 64; up to 8 for unmasked d = 128, where at 16 it was 3% slower).
+// and for d = 64; up to 8 for unmasked d = 128, where at 16 it was 3% slower; up to 32 for
+// causal d = 64, where 4x32x4096x64 ran in 324 instead of 341 us, while at 32 key tiles causal
+// d = 128 was 4% slower).
 constexpr int kPersistentMaxKvTiles = 16;
 __host__ __device__ constexpr bool use_persistent(int d, bool causal, int n_kvtiles) {
-  return n_kvtiles <= ((causal || d == 64) ? kPersistentMaxKvTiles : kPersistentMaxKvTiles / 2);
+  return n_kvtiles <= ((causal && d == 64) ? 2 * kPersistentMaxKvTiles
+                       : (causal || d == 64) ? kPersistentMaxKvTiles : kPersistentMaxKvTiles / 2);
 }
 
 template <int D>
@@ -1011,7 +1015,7 @@ fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {                                              // the whole warp (umma_*_w)
       const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
       const uint32_t idesc_o = idesc_bf16_f32(128, C::DO, 0, 1);
       const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 0, 1024);
@@ -1025,56 +1029,56 @@ fwd_persistent_kernel(const __grid_constant__ FwdParams p) {
 #pragma unroll
         for (int ks = 0; ks < C::KS_S; ++ks) {
           const uint32_t off = (ks >> 2) * C::CHUNK + (ks & 3) * 32;
-          umma_ss(tbase + C::T_S + t * 128, desc_advance(a, off), desc_advance(b, off), idesc_s, ks > 0);
+          umma_ss_w(tbase + C::T_S + t * 128, desc_advance(a, off), desc_advance(b, off), idesc_s, ks > 0);
         }
-        umma_commit(&s_full[t]);
+        umma_commit_w(&s_full[t]);
       };
       auto issue_pv = [&](int t, uint32_t P, bool first) {     // O_t += P_t V (position P)
         const uint64_t b = C::LB_MMA ? v_desc_ones(smem_u32(sV), (P % C::NS) * C::TILE, C::NS * C::TILE)
                                      : desc_advance(dv0, (P % C::NS) * C::TILE);
 #pragma unroll
         for (int ks = 0; ks < C::KS_PV; ++ks)
-          umma_ts(tbase + C::T_O + t * C::DO, tbase + C::T_S + t * 128 + ks * 8,
+          umma_ts_w(tbase + C::T_O + t * C::DO, tbase + C::T_S + t * 128 + ks * 8,
                   desc_advance(b, ks * 16 * 128), idesc_o, (!first || ks > 0) ? 1u : 0u);
       };
       uint32_t P = 0, cp[2] = {0, 0}, act[2] = {0, 0};
       bool ok = true;
       for (int k = 0; ok && pers_item(k, G) < p.n_items; ++k) {
         const FwdItem it = fwd_item(p, pers_item(k, G));
-        if (!(ok = mbar_wait(q_full, k & 1, abort_flag, 151) &&
-                   mbar_wait(&k_full[P % C::NS], (P / C::NS) & 1, abort_flag, 152)))
+        if (!(ok = mbar_wait_warp(q_full, k & 1, abort_flag, 151) &&
+                   mbar_wait_warp(&k_full[P % C::NS], (P / C::NS) & 1, abort_flag, 152)))
           break;
         tc_fence_after();
         // the S columns are free: the previous item's last PV products were issued before
         for (int t = 0; t < 2; ++t)
           if (it.n_t[t] > 0) issue_s(t, P);
-        umma_commit(&k_empty[P % C::NS]);
-        if (it.n_max == 1) umma_commit(q_empty);
+        umma_commit_w(&k_empty[P % C::NS]);
+        if (it.n_max == 1) umma_commit_w(q_empty);
         for (int j = 0; ok && j < it.n_max; ++j) {
           const uint32_t Pj = P + j;
           // V_j and K_{j+1} are loaded: the helper checked them before its p_full arrival
           for (int t = 0; t < 2; ++t) {
             if (j < it.n_t[t]) {
-              if (!(ok = mbar_wait(&p_full[t], cp[t] & 1, abort_flag, 153 + t))) break;
+              if (!(ok = mbar_wait_warp(&p_full[t], cp[t] & 1, abort_flag, 153 + t))) break;
               ++cp[t];
               // O_t of this tile's previous item has been read out by its epilogue
-              if (j == 0 && act[t] > 0 && !(ok = mbar_wait(&o_free[t], (act[t] - 1) & 1, abort_flag, 155 + t)))
+              if (j == 0 && act[t] > 0 && !(ok = mbar_wait_warp(&o_free[t], (act[t] - 1) & 1, abort_flag, 155 + t)))
                 break;
               tc_fence_after();
               issue_pv(t, Pj, j == 0);
-              if (j + 1 == it.n_t[t]) umma_commit(&o_done[t]);
+              if (j + 1 == it.n_t[t]) umma_commit_w(&o_done[t]);
             }
             if (j + 1 < it.n_t[t]) issue_s(t, Pj + 1);
           }
           if (!ok) break;
-          umma_commit(&v_empty[Pj % C::NS]);
-          if (j + 1 < it.n_max) umma_commit(&k_empty[(Pj + 1) % C::NS]);
-          if (j + 2 == it.n_max) umma_commit(q_empty);     // the item's last S products issued
+          umma_commit_w(&v_empty[Pj % C::NS]);
+          if (j + 1 < it.n_max) umma_commit_w(&k_empty[(Pj + 1) % C::NS]);
+          if (j + 2 == it.n_max) umma_commit_w(q_empty);     // the item's last S products issued
         }
         for (int t = 0; t < 2; ++t) act[t] += it.n_t[t] > 0;
         P += it.n_max;
       }
-      if (p.stats != nullptr) atomicAdd(&p.stats[0], n_s);
+      if (lane == 0 && p.stats != nullptr) atomicAdd(&p.stats[0], n_s);
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------------ helper

@@ -303,11 +303,96 @@ __device__ __forceinline__ void umma_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uin
       :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// Warp-issued forms.  The whole warp executes these, converged; `elect.sync` picks one lane
+// (with a full mask always the same one), which issues the product or the commit.  Measured on
+// this part (microbenchmark, one CTA on every SM, eight other warps running exponentials, FMA
+// chains and TMEM loads): products issued this way go out at the tensor rate (M=128, K=16:
+// 64 cycles at N=128, 37 at N=64 from TMEM), while the same products issued by one thread in a
+// single-lane branch take 85-91 cycles; alone, that thread needs >= 45 cycles a product.
+__device__ __forceinline__ void umma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P, E;\n\t"
+      "elect.sync _|E, 0xffffffff;\n\t"
+      "setp.ne.b32 P, %4, 0;\n\t"
+      "@E tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, P;\n\t}"
+      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+__device__ __forceinline__ void umma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P, E;\n\t"
+      "elect.sync _|E, 0xffffffff;\n\t"
+      "setp.ne.b32 P, %4, 0;\n\t"
+      "@E tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, P;\n\t}"
+      :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+__device__ __forceinline__ void umma_ss_f8_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P, E;\n\t"
+      "elect.sync _|E, 0xffffffff;\n\t"
+      "setp.ne.b32 P, %4, 0;\n\t"
+      "@E tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, P;\n\t}"
+      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+__device__ __forceinline__ void umma_ts_f8_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P, E;\n\t"
+      "elect.sync _|E, 0xffffffff;\n\t"
+      "setp.ne.b32 P, %4, 0;\n\t"
+      "@E tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, P;\n\t}"
+      :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+// The commit of the elected lane, which issued the warp's products (see umma_ss_w).
+__device__ __forceinline__ void umma_commit_w(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred E;\n\t"
+      "elect.sync _|E, 0xffffffff;\n\t"
+      "@E tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+      :: "r"(smem_u32(bar)) : "memory");
+}
+
 // Arrive once on ``bar`` when all previously issued tcgen05.mma of this thread complete.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
       :: "r"(smem_u32(bar)) : "memory");
+}
+
+// The two issue forms behind one name: W = true, the converged warp (umma_*_w); W = false,
+// the one thread that runs the issuing code (umma_ss and the rest).  The waits of the issuing
+// code follow the same choice (mbar_wait_by).
+template <bool W>
+__device__ __forceinline__ void umma_ss_by(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  if constexpr (W) umma_ss_w(d_tmem, a_desc, b_desc, idesc, accumulate);
+  else umma_ss(d_tmem, a_desc, b_desc, idesc, accumulate);
+}
+
+template <bool W>
+__device__ __forceinline__ void umma_ts_by(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  if constexpr (W) umma_ts_w(d_tmem, a_tmem, b_desc, idesc, accumulate);
+  else umma_ts(d_tmem, a_tmem, b_desc, idesc, accumulate);
+}
+
+template <bool W>
+__device__ __forceinline__ void umma_commit_by(uint64_t* bar) {
+  if constexpr (W) umma_commit_w(bar);
+  else umma_commit(bar);
+}
+
+template <bool W>
+__device__ __forceinline__ bool mbar_wait_by(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                             int where) {
+  if constexpr (W) return mbar_wait_warp(bar, parity, abort_flag, where);
+  else return mbar_wait(bar, parity, abort_flag, where);
 }
 
 __device__ __forceinline__ void tmem_wait_ld() {

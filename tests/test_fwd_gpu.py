@@ -135,15 +135,14 @@ def test_fwd_respects_stream():
     assert_o_close(o, o_ref)
 
 
-@pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("N", [1000, 2000])
+@pytest.mark.parametrize("causal,d,N", [(c, d, n) for c in (False, True) for d in (64, 128)
+                                          for n in (1000, 2000)] + [(True, 64, 3500)])
 def test_fwd_short_heads_many_items_per_cta(causal, d, N):
-    """Short heads (up to 16 key tiles causal or at d = 64, 8 otherwise) run on the persistent
-    forward, each CTA taking several work items (4 x 32 heads x 2 or 4 query pairs): it must
-    agree bit for bit with the one-CTA-per-item kernel, which the windowed entry point runs for
-    the same mask, and with the oracle on sampled heads.  (2000 unmasked at d = 128 runs the
-    one-CTA-per-item kernel on both sides.)"""
+    """Short heads (up to 32 key tiles causal at d = 64, 16 causal or at d = 64, 8 otherwise)
+    run on the persistent forward, each CTA taking several work items (4 x 32 heads x 2 to 7
+    query pairs): it must agree bit for bit with the one-CTA-per-item kernel, which the windowed
+    entry point runs for the same mask, and with the oracle on sampled heads.  (2000 unmasked at
+    d = 128 runs the one-CTA-per-item kernel on both sides.)"""
     require_gpu()
     B, H = 4, 32
     x = inputs.make_qkv(B, H, N, N, d, seed=77 + d, with_do=False)
