@@ -15,7 +15,8 @@
 //                 O_t += P_t V_j           A = P_t from TMEM, B = V_j from shared memory
 //               in the order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so the tensor core works
 //               on one tile while the other tile's softmax runs.
-//   warp 2      helper: folds "V_j loaded" and "K_{j+1} loaded" into the P hand-off (p_full), so
+//   warp 2      helper: folds "V_j loaded" and "K_{j+1} loaded" into the P hand-off (named barrier
+//               BAR_P + t in the plain and fp8 kernels, mbarrier p_full[t] otherwise), so
 //               the MMA thread waits once per tile and key tile (each wait of the issuing thread
 //               costs the tensor core a bubble).  Warp 3 is idle (warpgroup 0 gives up registers
 //               with setmaxnreg).
@@ -100,12 +101,13 @@ struct FwdCfg {
   // range (e4m3 is normal down to 2^-6).
   static constexpr float RESCALE_THRESHOLD = F8 ? 4.f : 8.f;
   static constexpr float P_BIAS = F8 ? 4.f : 0.f;
-  // fp8: the P hand-off of tile t is named barrier BAR_P + t (one generation per P V product:
-  // the tile's 128 softmax threads arrive, the MMA and helper warps sync).  An mbarrier wait
-  // costs the issuing thread ~150 cycles even when the phase is complete, which at the fp8
-  // tile rate leaves the tensor core idle; the hardware barrier does not.  (Measured: fp8
-  // 0.59 -> 0.56 ms; the bf16 forward was slower with it, so it keeps the mbarrier.)
-  static constexpr bool NAMED_P = F8;
+  // The P hand-off of tile t as named barrier BAR_P + t (one generation per P V product: the
+  // tile's 128 softmax threads arrive, the MMA and helper warps sync).  An mbarrier wait costs
+  // the issuing warp ~150 cycles even when the phase is complete; the hardware barrier does
+  // not.  Used by the fp8 forward (measured 0.59 -> 0.56 ms) and by the plain bf16 one (with
+  // the products issued by the converged warp: 4x32x4096x128 724 -> 716 us, causal 423 -> 416
+  // us; with one issuing thread it had been slower).  The varlen, window and block-sparse
+  // instantiations keep the mbarrier, whose waits are bounded.
   static constexpr uint32_t BAR_P = 3;
   static constexpr uint32_t BAR_P_THREADS = 128 + 32 + 32;
 };
@@ -165,6 +167,8 @@ struct FwdParams {
 template <int D, bool VL, bool F8 = false, bool WIN = false, bool BS = false>
 __global__ void __launch_bounds__(FwdCfg<D, F8>::THREADS, 1)
 fwd_kernel(const __grid_constant__ FwdParams p) {
+  // the P hand-off by named barrier (FwdCfg::BAR_P) in the fp8 and the plain bf16 forward
+  constexpr bool NAMED_P = F8 || (!VL && !WIN && !BS);
   using C = FwdCfg<D, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem_1k(smem_raw);
@@ -360,8 +364,8 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
         }
       }
     }
-  } else if (C::NAMED_P && warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer (fp8)
+  } else if (NAMED_P && warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer (named-barrier P hand-off)
     // The whole warp walks the loop (it takes part in the named-barrier hand-offs) and issues
     // (umma_*_w).  After a failed wait it keeps joining every hand-off, issuing nothing.
     if (n_max > 0) {
@@ -436,8 +440,8 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       }
       if (leader && p.stats != nullptr) atomicAdd(&p.stats[0], n_s);
     }
-  } else if (C::NAMED_P && warp == 2) {
-    // ------------------------------------------------------------------ helper (fp8)
+  } else if (NAMED_P && warp == 2) {
+    // ------------------------------------------------------------------ helper (named-barrier P hand-off)
     // Joins each P hand-off once V_j (and K_{j+1}, if an S(j+1) follows) is loaded, so the MMA
     // warp's single wait per hand-off also covers the loads.  The whole warp takes part; after
     // a failed wait it keeps joining every remaining hand-off.
@@ -748,7 +752,7 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
       lb += rb01.x + rb01.y;
       tmem_wait_st();
       tc_fence_before();
-      if constexpr (C::NAMED_P) {
+      if constexpr (NAMED_P) {
         __syncwarp();
         named_bar_arrive(C::BAR_P + t, C::BAR_P_THREADS);
         ++handed;
@@ -756,9 +760,10 @@ fwd_kernel(const __grid_constant__ FwdParams p) {
         mbar_arrive(&p_full[t]);
       }
     }
-    // fp8, after an abort: keep joining the remaining hand-offs (blocking, so these arrivals
-    // cannot run ahead of a generation the MMA and helper warps have not completed)
-    if constexpr (C::NAMED_P) {
+    // named-barrier hand-off, after an abort: keep joining the remaining ones (blocking, so
+    // these arrivals cannot run ahead of a generation the MMA and helper warps have not
+    // completed)
+    if constexpr (NAMED_P) {
       for (; handed < n; ++handed) {
         __syncwarp();
         named_bar_sync(C::BAR_P + t, C::BAR_P_THREADS);
