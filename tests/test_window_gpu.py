@@ -56,14 +56,17 @@ def test_window_zero_width_returns_v():
     assert torch.equal(o.cpu(), x["v"])
 
 
-@pytest.mark.parametrize("causal", [True, False])
-def test_window_special_cases_equal_the_plain_kernels(causal):
+@pytest.mark.parametrize("causal,d,N", [(True, 128, 1000), (False, 128, 1000), (True, 128, 2500),
+                                          (False, 128, 2500), (True, 64, 4500), (False, 64, 2200)])
+def test_window_special_cases_equal_the_plain_kernels(causal, d, N):
     """(-1, 0) is the causal mask and (-1, -1) no mask: the windowed kernel must reproduce the
-    causal / unmasked kernel bit for bit (same tiles, same arithmetic)."""
+    causal / unmasked kernel bit for bit (same tiles, same arithmetic).  At 1000 tokens the
+    plain call runs the persistent forward; the longer heads run the one-CTA-per-item kernel,
+    whose P hand-off is a named barrier where the windowed kernel's is an mbarrier."""
     require_gpu()
-    x = inputs.make_qkv(2, 3, 1000, 1000, 128, seed=6, with_do=False)
-    o_w, lse_w = run_fwd(x, -1, 0 if causal else -1, 128 ** -0.5)
-    o, lse = fa.forward(cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), causal=causal)
+    x = inputs.make_qkv(2, 3, N, N, d, seed=6, with_do=False)
+    o_w, lse_w = run_fwd(x, -1, 0 if causal else -1, d ** -0.5)
+    o, lse = fa.forward(cuda(x["q"]), cuda(x["k"]), cuda(x["v"]), causal=causal, scale=d ** -0.5)
     assert torch.equal(o_w, o)
     assert torch.equal(lse_w, lse)
 
