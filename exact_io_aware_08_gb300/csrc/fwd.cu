@@ -16,7 +16,7 @@
 //               in the order PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so the tensor core works
 //               on one tile while the other tile's softmax runs.
 //   warp 2      helper: folds "V_j loaded" and "K_{j+1} loaded" into the P hand-off (named barrier
-//               BAR_P + t in the plain and fp8 kernels, mbarrier p_full[t] otherwise), so
+//               BAR_P + t, mbarrier p_full[t] under a block mask), so
 //               the MMA thread waits once per tile and key tile (each wait of the issuing thread
 //               costs the tensor core a bubble).  Warp 3 is idle (warpgroup 0 gives up registers
 //               with setmaxnreg).
@@ -106,8 +106,9 @@ struct FwdCfg {
   // the issuing warp ~150 cycles even when the phase is complete; the hardware barrier does
   // not.  Used by the fp8 forward (measured 0.59 -> 0.56 ms) and by the plain bf16 one (with
   // the products issued by the converged warp: 4x32x4096x128 724 -> 716 us, causal 423 -> 416
-  // us; with one issuing thread it had been slower).  The varlen, window and block-sparse
-  // instantiations keep the mbarrier, whose waits are bounded.
+  // us; with one issuing thread it had been slower), the varlen one (2.54 -> 2.49 ms on 16
+  // causal sequences of 512-8192 tokens) and the windowed one.  The block-sparse
+  // instantiation, whose tiles skip steps, keeps the mbarrier, whose waits are bounded.
   static constexpr uint32_t BAR_P = 3;
   static constexpr uint32_t BAR_P_THREADS = 128 + 32 + 32;
 };
@@ -167,8 +168,8 @@ struct FwdParams {
 template <int D, bool VL, bool F8 = false, bool WIN = false, bool BS = false>
 __global__ void __launch_bounds__(FwdCfg<D, F8>::THREADS, 1)
 fwd_kernel(const __grid_constant__ FwdParams p) {
-  // the P hand-off by named barrier (FwdCfg::BAR_P) in the fp8 and the plain bf16 forward
-  constexpr bool NAMED_P = F8 || (!VL && !WIN && !BS);
+  // the P hand-off by named barrier (FwdCfg::BAR_P), except under a block mask
+  constexpr bool NAMED_P = F8 || !BS;
   using C = FwdCfg<D, F8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem_1k(smem_raw);
